@@ -1,0 +1,309 @@
+"""Seeded synthetic workloads for the MiniMax Sparse Attention (MSA) hot path.
+
+This module is shared by the CPU oracle tests, the CUDA parity tests and the
+benchmark.  It holds no arithmetic of the method itself: only random draws,
+page placement in a shared pool, and the planted "needle" structure that makes
+block selection non-trivial.  Everything is a pure function of the seed.
+
+Layouts (one physical pool, pages of 128 tokens, token stride = groups * dim,
+as in the strided paged-KV view of "将 MSA 与分页注意力集成" on the Together AI
+page "Together AI 解析如何高效服务 MiniMax M3：1M token 上下文与多模态推理优化"):
+
+    k_cache, v_cache : bf16 [n_pages][page][G][D]
+    kidx_cache       : bf16 [n_pages][page][G][Di]   (same page ids as K/V)
+    block_table      : int32 [n_req][max_blocks]     logical block -> page, -1 = none
+    seq_lens         : int32 [n_req]                 tokens in the cache, incl. new ones
+    q                : bf16 [rows][Hq][D]
+    q_idx            : bf16 [rows][G][Di]
+    q_req, q_pos     : int32 [rows]                  request and absolute position
+
+Values are drawn in fp32 from N(0, 1) and rounded to bf16 (round-to-nearest-even,
+torch's conversion).  A needle adds 3 * u to the fp32 index keys of every token of
+one (block, group) before rounding, where u is a unit vector along the query-side
+index direction of that group.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+PAGE = 128
+
+__all__ = [
+    "PAGE", "Dims", "Case", "decode_case", "prefill_case", "tiny_case",
+    "ragged_lengths", "named_case", "CONFIG_NAMES",
+]
+
+
+@dataclass(frozen=True)
+class Dims:
+    Hq: int
+    G: int
+    D: int
+    Di: int
+    topk: int
+    page: int = PAGE
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+@dataclass
+class Case:
+    """One synthetic workload: a paged cache plus query rows."""
+    dims: Dims
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    kidx_cache: torch.Tensor
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    q: torch.Tensor
+    q_idx: torch.Tensor
+    q_req: torch.Tensor
+    q_pos: torch.Tensor
+    max_blocks: int
+    needles: List[Tuple[int, int, int]] = field(default_factory=list)  # (req, group, block)
+    name: str = ""
+
+    @property
+    def n_pages(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def n_req(self) -> int:
+        return int(self.block_table.shape[0])
+
+    def to(self, device) -> "Case":
+        out = Case(**{k: (v.to(device) if isinstance(v, torch.Tensor) else v)
+                      for k, v in self.__dict__.items()})
+        return out
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn_f32(shape, gen, device) -> torch.Tensor:
+    return torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32)
+
+
+def _pool_bf16(n_pages: int, page: int, G: int, width: int, gen, device,
+               shifts: Optional[dict] = None) -> torch.Tensor:
+    """Draw a paged pool chunk by chunk; `shifts` maps page -> [(group, fp32 vector)]
+    added to every token of that (page, group) before the bf16 rounding."""
+    out = torch.empty((n_pages, page, G, width), dtype=torch.bfloat16, device=device)
+    per_page = page * G * width
+    step = max(1, (1 << 25) // per_page)
+    for p0 in range(0, n_pages, step):
+        n = min(step, n_pages - p0)
+        x = _randn_f32((n, page, G, width), gen, device)
+        if shifts:
+            for p in range(p0, p0 + n):
+                for (grp, vec) in shifts.get(p, ()):
+                    x[p - p0, :, grp, :] += vec.to(device)
+        out[p0:p0 + n] = x.to(torch.bfloat16)
+    return out
+
+
+def _place_pages(lens: Sequence[int], pool_pages: int, page: int, gen_cpu) -> Tuple[torch.Tensor, int]:
+    n_blk = [(L + page - 1) // page for L in lens]
+    total = sum(n_blk)
+    if total > pool_pages:
+        raise ValueError(f"pool of {pool_pages} pages cannot hold {total} blocks")
+    max_blocks = max(n_blk)
+    perm = torch.randperm(pool_pages, generator=gen_cpu)
+    bt = torch.full((len(lens), max_blocks), -1, dtype=torch.int32)
+    cur = 0
+    for b, nb in enumerate(n_blk):
+        bt[b, :nb] = perm[cur:cur + nb].to(torch.int32)
+        cur += nb
+    return bt, max_blocks
+
+
+def _unit(v: torch.Tensor) -> torch.Tensor:
+    n = torch.linalg.vector_norm(v)
+    return v / n if float(n) > 0 else v
+
+
+def _pick_needles(n_cand_excl_own: int, count: int, gen_cpu,
+                  ranges: Optional[Sequence[Tuple[int, int, int]]] = None) -> List[int]:
+    """Distinct block ids in [0, n_cand_excl_own).  `ranges` = [(lo, hi, count)] overrides
+    the uniform draw (used for the 1M-token placement at the start, middle and end)."""
+    if n_cand_excl_own <= 0:
+        return []
+    if ranges is None:
+        count = min(count, n_cand_excl_own)
+        return sorted(torch.randperm(n_cand_excl_own, generator=gen_cpu)[:count].tolist())
+    picked: List[int] = []
+    for lo, hi, c in ranges:
+        hi = min(hi, n_cand_excl_own)
+        lo = max(0, min(lo, hi))
+        if hi <= lo:
+            continue
+        cand = torch.randperm(hi - lo, generator=gen_cpu)[:min(c, hi - lo)] + lo
+        picked.extend(int(x) for x in cand.tolist())
+    return sorted(set(picked))
+
+
+def decode_case(lens: Sequence[int], Hq: int, G: int, D: int, Di: int, topk: int,
+                pool_pages: int, needles_per_group: int, seed: int, device="cpu",
+                needle_ranges_frac: Optional[Sequence[Tuple[float, float, int]]] = None,
+                name: str = "") -> Case:
+    """Decode batch: request b holds lens[b] cached tokens (incl. the new one); one
+    query row per request at position lens[b] - 1.  Needles sit in blocks other than
+    the query's own block, shifted along u = q_idx[b, g] / |q_idx[b, g]|."""
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages(lens, pool_pages, page, gc)
+    B = len(lens)
+    gd = _gen(seed + 7919, device)
+    q = _randn_f32((B, Hq, D), gd, device).to(torch.bfloat16)
+    q_idx = _randn_f32((B, G, Di), gd, device).to(torch.bfloat16)
+    shifts: dict = {}
+    needles: List[Tuple[int, int, int]] = []
+    qi_cpu = q_idx.float().cpu()
+    for b, L in enumerate(lens):
+        own = (L - 1) // page
+        for g in range(G):
+            if needle_ranges_frac is not None:
+                nb = (L + page - 1) // page
+                ranges = [(int(math.floor(lo * nb)), int(math.ceil(hi * nb)), c)
+                          for (lo, hi, c) in needle_ranges_frac]
+                blocks = _pick_needles(own, 0, gc, ranges)
+            else:
+                blocks = _pick_needles(own, needles_per_group, gc)
+            u = _unit(qi_cpu[b, g])
+            for j in blocks:
+                p = int(bt[b, j])
+                shifts.setdefault(p, []).append((g, 3.0 * u))
+                needles.append((b, g, j))
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device, shifts)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    seq = torch.tensor(list(lens), dtype=torch.int32)
+    return Case(dims, k_cache, v_cache, kidx, bt.to(device), seq.to(device), q, q_idx,
+                torch.arange(B, dtype=torch.int32, device=device),
+                (seq - 1).to(torch.int32).to(device), max_blocks, needles, name)
+
+
+def prefill_case(prefix: int, chunk: int, Hq: int, G: int, D: int, Di: int, topk: int,
+                 pool_pages: int, seed: int, device="cpu", span: int = 256,
+                 span_sigma: float = 0.5, name: str = "") -> Case:
+    """Chunked prefill of one request: `chunk` new query rows at positions
+    prefix .. prefix+chunk-1 over a cache of prefix+chunk tokens (the chunk's own
+    K/V/index keys already appended).  Query-side index vectors of rows in the same
+    `span`-token window are drawn around a shared centre c ~ N(0, 1) per (window,
+    group): q_idx = c + span_sigma * N(0, 1), so many rows pick the same blocks."""
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    L = prefix + chunk
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages([L], pool_pages, page, gc)
+    gd = _gen(seed + 7919, device)
+    q = _randn_f32((chunk, Hq, D), gd, device).to(torch.bfloat16)
+    n_span = (chunk + span - 1) // span
+    centres = _randn_f32((n_span, G, Di), gd, device)
+    noise = _randn_f32((chunk, G, Di), gd, device)
+    span_of_row = torch.arange(chunk, device=device) // span
+    q_idx = (centres[span_of_row] + span_sigma * noise).to(torch.bfloat16)
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    pos = torch.arange(prefix, L, dtype=torch.int32, device=device)
+    return Case(dims, k_cache, v_cache, kidx, bt.to(device),
+                torch.tensor([L], dtype=torch.int32, device=device), q, q_idx,
+                torch.zeros(chunk, dtype=torch.int32, device=device), pos, max_blocks, [], name)
+
+
+def tiny_case(seed: int = 1000, device="cpu", L: int = 2048, n_decode: int = 16,
+              Hq: int = 8, G: int = 2, D: int = 64, Di: int = 32, topk: int = 4,
+              pool_pages: int = 32, needles_per_group: int = 2) -> Tuple[Case, Case]:
+    """Small prefill + decode pair over ONE cache.
+
+    The cache holds L + n_decode tokens.  The prefill case has rows at positions
+    0 .. L-1 (causal).  The decode case has n_decode rows, one per decode step, at
+    positions L .. L+n_decode-1; all rows share request 0's pages, and row i sees
+    seq_len L+i+1 (equivalent to appending one token per step, since a row never
+    attends past its own position).  Needles: `needles_per_group` blocks per group,
+    shifted along u_g = unit(mean over the prefill rows of q_idx[:, g])."""
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    total = L + n_decode
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages([total], pool_pages, page, gc)
+    gd = _gen(seed + 7919, device)
+    q = _randn_f32((total, Hq, D), gd, device).to(torch.bfloat16)
+    q_idx = _randn_f32((total, G, Di), gd, device).to(torch.bfloat16)
+    qi_cpu = q_idx[:L].float().cpu()
+    shifts: dict = {}
+    needles: List[Tuple[int, int, int]] = []
+    n_full = L // page
+    for g in range(G):
+        u = _unit(qi_cpu[:, g, :].mean(dim=0))
+        for j in _pick_needles(max(n_full - 1, 0), needles_per_group, gc):
+            shifts.setdefault(int(bt[0, j]), []).append((g, 3.0 * u))
+            needles.append((0, g, j))
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device, shifts)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    btd = bt.to(device)
+    pre = Case(dims, k_cache, v_cache, kidx, btd,
+               torch.tensor([total], dtype=torch.int32, device=device),
+               q[:L].contiguous(), q_idx[:L].contiguous(),
+               torch.zeros(L, dtype=torch.int32, device=device),
+               torch.arange(L, dtype=torch.int32, device=device), max_blocks, needles, "tiny-prefill")
+    dec_bt = btd.expand(n_decode, -1).contiguous()
+    lens = torch.arange(L + 1, L + n_decode + 1, dtype=torch.int32, device=device)
+    dec = Case(dims, k_cache, v_cache, kidx, dec_bt, lens,
+               q[L:].contiguous(), q_idx[L:].contiguous(),
+               torch.arange(n_decode, dtype=torch.int32, device=device),
+               (lens - 1).to(torch.int32), max_blocks, needles, "tiny-decode")
+    return pre, dec
+
+
+def ragged_lengths(B: int, seed: int, lo: int = 4096, hi: int = 131072) -> List[int]:
+    """Per-request context lengths drawn log-uniform in [lo, hi] (seeded)."""
+    g = _gen(seed, "cpu")
+    u = torch.rand(B, generator=g, dtype=torch.float64)
+    return [int(round(math.exp(math.log(lo) + float(x) * (math.log(hi) - math.log(lo))))) for x in u]
+
+
+CONFIG_NAMES = ("tiny", "decode60k", "prefill68k", "ragged1", "ragged8", "ragged32",
+                "ragged64", "decode1m")
+
+
+def named_case(name: str, device="cpu"):
+    """The five named workloads (seed 1000 + workload number).  "tiny" returns a
+    (prefill, decode) pair; the others return one Case."""
+    H = dict(Hq=64, G=8, D=128, Di=64, topk=16)
+    if name == "tiny":
+        return tiny_case(seed=1000, device=device)
+    if name == "decode60k":
+        return decode_case([60000] * 8, pool_pages=4096, needles_per_group=4,
+                           seed=1001, device=device, name=name, **H)
+    if name == "prefill68k":
+        return prefill_case(60000, 8192, pool_pages=4096, seed=1002, device=device,
+                            name=name, **H)
+    if name.startswith("ragged"):
+        B = int(name[len("ragged"):])
+        lens = ragged_lengths(B, seed=1003 + B)
+        pool = int(math.ceil(1.25 * sum((L + PAGE - 1) // PAGE for L in lens)))
+        return decode_case(lens, pool_pages=pool, needles_per_group=4, seed=1003,
+                           device=device, name=name, **H)
+    if name == "decode1m":
+        ranges = [(0.0, 0.05, 3), (0.475, 0.525, 3), (0.95, 1.0, 2)]
+        return decode_case([1 << 20] * 2, pool_pages=16640, needles_per_group=8,
+                           seed=1004, device=device, needle_ranges_frac=ranges,
+                           name=name, **H)
+    raise KeyError(name)
