@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA hot path on GB300; prints ONE JSON line on rank 0.
+
+Headline: MSA decode at the agentic shape (8 requests x 60,000 cached tokens,
+Hq=64, G=8, D=128, Di=64, top-16 blocks of 128 tokens): one step = index scoring
+-> top-k -> page tables -> paged sparse attention for the whole batch.  The
+prefill chunk (8,192 new rows on a 60,000-token prefix) is timed the same way and
+reported in the "prefill" object of the same line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl msa|reference]
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own batch: weak
+scaling, no collective on the data path; the time is the max over ranks.
+--impl reference times the fp64 CPU oracle on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MSA decode tok/s & prefill q-tok/s at 60k ctx; % of HBM / tensor-core roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per launch from the committed ncu summaries; None
+# until a capture of the current kernel exists.
+NCU_TRAFFIC = {"k_score_decode": None, "k_attn_prefill": None}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-benchmark")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (the job's wall time is the slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="msa_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "-i", str(self.idx),
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def decode_bytes(case) -> int:
+    """Algorithmic bytes of one decode step's index scan: every cached token's
+    index key of every group is read once (L * G * Di * 2 per request)."""
+    d = case.dims
+    return int(sum(int(L) for L in case.seq_lens.tolist()) * d.G * d.Di * 2)
+
+
+def prefill_attention_flops(step, case) -> float:
+    """Algorithmic flops of block-major attention: 4 * D per (query head, attended token)."""
+    import torch
+    d = case.dims
+    sel = step.sel.long()
+    pos = case.q_pos.long()[:, None, None]
+    vis = (pos - sel * 128 + 1).clamp(min=0, max=128)
+    vis = torch.where(sel >= 0, vis, torch.zeros_like(vis))
+    hpg = d.Hq // d.G
+    return float(vis.sum().item()) * hpg * 4 * d.D
+
+
+def run_msa(args, rank, world, local):
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    peaks, peak_src = load_peaks()
+    K, W = args.steps, args.warmup
+
+    # ---------------- decode headline
+    case = mi.named_case("decode60k", device=dev)
+    dims = msa.dims_of(case)
+    B = case.n_rows
+    step = msa.DecodeStep(dims, B, case.n_req, case.n_pages, dev)
+    call = lambda: step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table,
+                        case.seq_lens, case.q_pos)
+    for _ in range(W):
+        call()
+    msa.msa_check(step.err)
+    torch.cuda.synchronize()
+    s1_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    s1_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local).start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record()
+    for k in range(K):
+        s1_b[k].record()
+        step.scores_only(case.q_idx, case.kidx_cache, case.block_table, case.q_pos)
+        s1_e[k].record()
+        step.rest(case.q, case.k_cache, case.v_cache, case.block_table, case.q_pos, case.seq_lens)
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    dec_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    s1_ms = statistics.mean(s1_b[k].elapsed_time(s1_e[k]) for k in range(K))
+    msa.msa_check(step.err)
+    value = aggregate_throughput(B * K, world, dec_ms / 1e3)
+    s1_bytes = decode_bytes(case)
+    s1_gbs = s1_bytes / (s1_ms / 1e3) / 1e9
+
+    # ---------------- e2e through the public API: pinned host inputs in, result out
+    host_in = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table")}
+    dev_in = {n: torch.empty_like(getattr(case, n)) for n in host_in}
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        out, lse = step(dev_in["q"], dev_in["q_idx"], case.k_cache, case.v_cache, case.kidx_cache,
+                        dev_in["block_table"], dev_in["seq_lens"], dev_in["q_pos"])
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(W):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    msa.msa_check(step.err)
+    e2e_value = aggregate_throughput(B * K, world, e2e_ms / 1e3)
+
+    # ---------------- prefill chunk
+    prefill = None
+    if not args.no_prefill:
+        del step, case
+        torch.cuda.empty_cache()
+        pc = mi.named_case("prefill68k", device=dev)
+        pd = msa.dims_of(pc)
+        ps = msa.PrefillStep(pd, pc.n_rows, pc.n_req, dev)
+        pcall = lambda: ps(pc.q, pc.q_idx, pc.k_cache, pc.v_cache, pc.kidx_cache, pc.block_table, pc.q_req,
+                           pc.q_pos)
+        for _ in range(W):
+            pcall()
+        msa.msa_check(ps.err)
+        torch.cuda.synchronize()
+        a_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        a_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        p0.record()
+        for k in range(K):
+            ps.select(pc.q_idx, pc.kidx_cache, pc.block_table, pc.q_req, pc.q_pos)
+            a_b[k].record()
+            msa.msa_sparse_attn_prefill(pc.q, pc.k_cache, pc.v_cache, pc.block_table, pc.q_req, pc.q_pos,
+                                        ps.blk_off, ps.blk_ent, pd, ps.o_part, ps.lse_part, err_word=ps.err)
+            a_e[k].record()
+            msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, pd, ps.out, ps.lse, err_word=ps.err)
+        p1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        pre_ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
+        attn_ms = statistics.mean(a_b[k].elapsed_time(a_e[k]) for k in range(K))
+        msa.msa_check(ps.err)
+        flops = prefill_attention_flops(ps, pc)
+        tflops = flops / (attn_ms / 1e3) / 1e12
+        prefill = {
+            "metric": "MSA prefill q-tok/s", "value": aggregate_throughput(pc.n_rows * K, world, pre_ms / 1e3),
+            "unit": "q-tok/s", "ms_per_step": pre_ms / K, "steps": K,
+            "config": {"workload": "prefill68k", "prefix": 60000, "chunk": pc.n_rows, "Hq": pd.Hq, "G": pd.G,
+                       "D": pd.D, "Di": pd.Di, "topk": pd.topk},
+            "gpu_launches": ps.kernel_launches * K,
+            "roofline": {"bound": "tensor", "kernel": "k_attn_prefill", "achieved": tflops,
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tflops / peaks["bf16_tflops"], "traffic": NCU_TRAFFIC["k_attn_prefill"],
+                         "flops_per_launch": flops, "ms_per_launch": attn_ms,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        }
+    clk = clocks.stop()
+
+    # ---------------- CPU baseline: the oracle on host cores, bounded sample
+    cpu = cpu_baseline_decode(rank) if rank == 0 else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": dec_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, planted needle blocks)",
+        "config": {"workload": "decode60k", "batch": B, "ctx": 60000, "Hq": dims.Hq, "G": dims.G, "D": dims.D,
+                   "Di": dims.Di, "topk": dims.topk, "page": 128, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (491.5 MB k-index scan per step)"},
+        "gpu_launches": step_launches_decode() * K,
+        "roofline": {"bound": "hbm", "kernel": "k_score_decode", "achieved": s1_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": s1_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC["k_score_decode"],
+                     "bytes_per_launch": s1_bytes, "ms_per_launch": s1_ms,
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / K},
+        "clocks": clk,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def step_launches_decode() -> int:
+    return 5   # score, top-k, page table, attention partials, merge
+
+
+# ------------------------------------------------------------------ oracle legs (CPU)
+
+def _oracle_decode_one(case, b):
+    """The fp64 oracle's decode of request b (scores, top-k, page table, attention),
+    on host copies of just the pages it reads.  Returns the oracle's CPU seconds."""
+    import torch
+    import oracle
+    bt = case.block_table[b:b + 1].cpu()
+    pages = bt[bt >= 0].long()
+    kidx = case.kidx_cache[pages.to(case.kidx_cache.device)].cpu()
+    bt_c = torch.full_like(bt, -1)
+    bt_c[bt >= 0] = torch.arange(len(pages), dtype=torch.int32)
+    q_pos = case.q_pos[b:b + 1].cpu()
+    local = torch.zeros(1, dtype=torch.int32)
+    t = time.perf_counter()
+    sc = oracle.block_scores(case.q_idx[b:b + 1].cpu(), kidx, bt_c, local, q_pos, case.max_blocks)
+    sel = oracle.topk(sc, q_pos, case.dims.topk)
+    t_sel = time.perf_counter() - t
+    used = sorted({int(bt[0, j]) for j in sel.flatten().tolist() if j >= 0})
+    remap = {p: i for i, p in enumerate(used)}
+    kc = case.k_cache[torch.tensor(used, device=case.k_cache.device)].cpu()
+    vc = case.v_cache[torch.tensor(used, device=case.v_cache.device)].cpu()
+    bt_a = torch.tensor([[remap.get(int(p), 0) for p in bt[0].tolist()]], dtype=torch.int32)
+    t = time.perf_counter()
+    pt, rl = oracle.page_table(sel, bt_a, q_pos + 1)
+    oracle.paged_attention(case.q[b:b + 1].cpu(), kc, vc, pt, rl, case.dims.sm_scale)
+    return t_sel + time.perf_counter() - t
+
+
+def cpu_baseline_decode(rank: int, budget_s: float = 12.0, max_reqs: int = 1000, case=None):
+    import torch
+    import msa_inputs as mi
+    if case is None:
+        dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+        case = mi.named_case("decode60k", device=dev)
+    spent, n = 0.0, 0
+    while spent < budget_s and n < max_reqs:
+        spent += _oracle_decode_one(case, n % case.n_rows)
+        n += 1
+    return {"value": n / spent, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "host_cores": os.cpu_count(),
+            "sample": f"{n} decode requests of the decode60k workload (60,000 cached tokens each), "
+                      f"single-threaded fp64 C oracle, {spent:.1f} s of CPU time"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: rank 0 only, a bounded sample per step."""
+    if rank != 0:
+        return
+    import torch
+    import msa_inputs as mi
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    case = mi.named_case("decode60k", device=dev)
+    for i in range(args.warmup):
+        _oracle_decode_one(case, i % case.n_rows)
+    spent = 0.0
+    for k in range(args.steps):
+        spent += _oracle_decode_one(case, k % case.n_rows)
+    value = args.steps / spent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, planted needle blocks)",
+        "config": {"workload": "decode60k", "batch": case.n_rows, "ctx": 60000, "Hq": 64, "G": 8, "D": 128,
+                   "Di": 64, "topk": 16, "page": 128, "parallelism": "single host thread"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "kind": "oracle", "cores": 1,
+                         "sample": "each step = the full decode of one request of decode60k "
+                                   "(60,000-token index scan, top-16, attention over 2,016 tokens), "
+                                   "single-threaded fp64 C oracle"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_msa(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,383 @@
+"""MiniMax Sparse Attention (MSA) hot path for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over libmsa.so (C ABI in include/msa.h).  Every function
+here only marshals arguments: it checks dtypes, shapes and devices, allocates
+outputs with torch when the caller passes none, and calls the C entry point of
+the same name on torch's current CUDA stream.  All arithmetic runs in the CUDA
+kernels; there is no CPU path.  Importing this package without the built
+library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmsa.so")
+
+MSA_PHASE_DECODE = 0
+MSA_PHASE_PREFILL = 1
+MSA_OP_INVERT = 0
+MSA_OP_DECODE = 1
+
+STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
+          4: "MSA_ERR_DEVICE_BOUNDS", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_WORKSPACE",
+          7: "MSA_ERR_DEVICE_UNSUPPORTED"}
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class msa_dims_t(ctypes.Structure):
+    _fields_ = [("Hq", ctypes.c_int32), ("G", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("Di", ctypes.c_int32), ("page_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+
+
+@dataclass(frozen=True)
+class Dims:
+    Hq: int
+    G: int
+    D: int
+    Di: int
+    topk: int
+    max_blocks: int
+    sm_scale: Optional[float] = None
+    page_size: int = 128
+
+    def c(self) -> msa_dims_t:
+        sc = self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(self.D)
+        return msa_dims_t(self.Hq, self.G, self.D, self.Di, self.page_size, self.topk, self.max_blocks, sc)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmsa.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                          "or python -m block_sparse_attention_06_gb300._build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.POINTER(msa_dims_t)
+    sigs = {
+        "msa_index_score": [P, P, P, P, P, I, I, I, D, I, P, P, P],
+        "msa_topk_blocks": [P, P, I, D, P, P, P],
+        "msa_build_page_table": [P, P, P, I, I, D, P, P, P, P],
+        "msa_invert_selection": [P, P, I, I, D, P, P, P, S, P, P],
+        "msa_sparse_attn_prefill": [P, P, P, P, P, P, P, P, I, I, I, D, P, P, P, P],
+        "msa_lse_merge": [P, P, P, I, D, P, P, P, P],
+        "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
+        "msa_check": [P, P],
+    }
+    for name, argt in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = argt
+        fn.restype = ctypes.c_int
+    lib.msa_workspace_bytes.argtypes = [I, I, I, D]
+    lib.msa_workspace_bytes.restype = ctypes.c_size_t
+    lib.msa_last_error.restype = ctypes.c_char_p
+    lib.msa_last_error.argtypes = []
+    lib.msa_status_str.restype = ctypes.c_char_p
+    lib.msa_status_str.argtypes = [ctypes.c_int]
+    lib.msa_version.restype = ctypes.c_int32
+    lib.msa_version.argtypes = []
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _call(name: str, *args):
+    rc = getattr(_lib, name)(*args)
+    if rc != 0:
+        raise MsaError(rc, name, _lib.msa_last_error().decode(errors="replace"))
+
+
+def _req(t: torch.Tensor, dtype, name: str, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def new_err_word(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def msa_check(err_word: torch.Tensor) -> None:
+    """Synchronise the current stream, raise MsaError if a kernel flagged an error, clear the word."""
+    _req(err_word, torch.int32, "err_word")
+    _call("msa_check", _ptr(err_word), _stream(err_word.device))
+
+
+def msa_workspace_bytes(op: int, n_rows: int, n_req: int, dims: Dims) -> int:
+    d = dims.c()
+    return int(_lib.msa_workspace_bytes(op, n_rows, n_req, ctypes.byref(d)))
+
+
+def msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, dims: Dims, phase: int,
+                    scores=None, err_word=None):
+    n_rows = q_idx.shape[0]
+    _req(q_idx, torch.bfloat16, "q_idx", (n_rows, dims.G, dims.Di))
+    _req(kidx_cache, torch.bfloat16, "kidx_cache")
+    if kidx_cache.dim() != 4 or tuple(kidx_cache.shape[1:]) != (dims.page_size, dims.G, dims.Di):
+        raise ValueError("kidx_cache must be [n_pages][128][G][Di]")
+    _req(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or block_table.shape[1] != dims.max_blocks:
+        raise ValueError("block_table must be [n_req][max_blocks]")
+    _req(q_req, torch.int32, "q_req", (n_rows,))
+    _req(q_pos, torch.int32, "q_pos", (n_rows,))
+    dev = q_idx.device
+    if scores is None:
+        scores = torch.empty((n_rows, dims.G, dims.max_blocks), dtype=torch.float32, device=dev)
+    _req(scores, torch.float32, "scores", (n_rows, dims.G, dims.max_blocks))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_index_score", _ptr(q_idx), _ptr(kidx_cache), _ptr(block_table), _ptr(q_req), _ptr(q_pos),
+          n_rows, block_table.shape[0], kidx_cache.shape[0], ctypes.byref(d), phase, _ptr(scores),
+          _ptr(err_word), _stream(dev))
+    return scores
+
+
+def msa_topk_blocks(scores, q_pos, dims: Dims, sel=None, err_word=None):
+    n_rows = scores.shape[0]
+    _req(scores, torch.float32, "scores", (n_rows, dims.G, dims.max_blocks))
+    _req(q_pos, torch.int32, "q_pos", (n_rows,))
+    dev = scores.device
+    if sel is None:
+        sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, device=dev)
+    _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_topk_blocks", _ptr(scores), _ptr(q_pos), n_rows, ctypes.byref(d), _ptr(sel), _ptr(err_word),
+          _stream(dev))
+    return sel
+
+
+def msa_build_page_table(sel, block_table, seq_lens, n_pages: int, dims: Dims, page_table=None, row_len=None,
+                         err_word=None):
+    B = sel.shape[0]
+    _req(sel, torch.int32, "sel", (B, dims.G, dims.topk))
+    _req(block_table, torch.int32, "block_table", (B, dims.max_blocks))
+    _req(seq_lens, torch.int32, "seq_lens", (B,))
+    dev = sel.device
+    if page_table is None:
+        page_table = torch.empty((B * dims.G, dims.topk), dtype=torch.int32, device=dev)
+    if row_len is None:
+        row_len = torch.empty((B * dims.G,), dtype=torch.int32, device=dev)
+    _req(page_table, torch.int32, "page_table", (B * dims.G, dims.topk))
+    _req(row_len, torch.int32, "row_len", (B * dims.G,))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_build_page_table", _ptr(sel), _ptr(block_table), _ptr(seq_lens), B, n_pages, ctypes.byref(d),
+          _ptr(page_table), _ptr(row_len), _ptr(err_word), _stream(dev))
+    return page_table, row_len
+
+
+def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_ent=None, workspace=None,
+                         err_word=None):
+    n_rows = sel.shape[0]
+    _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    _req(q_req, torch.int32, "q_req", (n_rows,))
+    dev = sel.device
+    n_keys = dims.G * n_req * dims.max_blocks
+    if blk_off is None:
+        blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, device=dev)
+    if blk_ent is None:
+        blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, device=dev)
+    _req(blk_off, torch.int32, "blk_off", (n_keys + 1,))
+    _req(blk_ent, torch.int32, "blk_ent")
+    if blk_ent.numel() < n_rows * dims.G * dims.topk:
+        raise ValueError("blk_ent too small")
+    need = msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    _req(workspace, torch.uint8, "workspace")
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_invert_selection", _ptr(sel), _ptr(q_req), n_rows, n_req, ctypes.byref(d), _ptr(blk_off),
+          _ptr(blk_ent), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
+    return blk_off, blk_ent
+
+
+def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, dims: Dims,
+                            o_part=None, lse_part=None, err_word=None):
+    n_rows = q.shape[0]
+    _req(q, torch.bfloat16, "q", (n_rows, dims.Hq, dims.D))
+    _req(k_cache, torch.bfloat16, "k_cache")
+    _req(v_cache, torch.bfloat16, "v_cache", tuple(k_cache.shape))
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (dims.page_size, dims.G, dims.D):
+        raise ValueError("k_cache must be [n_pages][128][G][D]")
+    _req(block_table, torch.int32, "block_table")
+    n_req = block_table.shape[0]
+    _req(q_req, torch.int32, "q_req", (n_rows,))
+    _req(q_pos, torch.int32, "q_pos", (n_rows,))
+    _req(blk_off, torch.int32, "blk_off", (dims.G * n_req * dims.max_blocks + 1,))
+    _req(blk_ent, torch.int32, "blk_ent")
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((n_rows, dims.topk, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, device=dev)
+    _req(o_part, torch.bfloat16, "o_part", (n_rows, dims.topk, dims.Hq, dims.D))
+    _req(lse_part, torch.float32, "lse_part", (n_rows, dims.topk, dims.Hq))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_sparse_attn_prefill", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(q_req),
+          _ptr(q_pos), _ptr(blk_off), _ptr(blk_ent), n_rows, n_req, k_cache.shape[0], ctypes.byref(d),
+          _ptr(o_part), _ptr(lse_part), _ptr(err_word), _stream(dev))
+    return o_part, lse_part
+
+
+def msa_lse_merge(o_part, lse_part, sel, dims: Dims, out=None, lse=None, err_word=None):
+    n_rows = o_part.shape[0]
+    _req(o_part, torch.bfloat16, "o_part", (n_rows, dims.topk, dims.Hq, dims.D))
+    _req(lse_part, torch.float32, "lse_part", (n_rows, dims.topk, dims.Hq))
+    _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    dev = o_part.device
+    if out is None:
+        out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, device=dev)
+    _req(out, torch.bfloat16, "out", (n_rows, dims.Hq, dims.D))
+    _req(lse, torch.float32, "lse", (n_rows, dims.Hq))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_lse_merge", _ptr(o_part), _ptr(lse_part), _ptr(sel), n_rows, ctypes.byref(d), _ptr(out),
+          _ptr(lse), _ptr(err_word), _stream(dev))
+    return out, lse
+
+
+def msa_sparse_attn_decode(q, k_cache, v_cache, page_table, row_len, dims: Dims, out=None, lse=None,
+                           workspace=None, err_word=None):
+    B = q.shape[0]
+    _req(q, torch.bfloat16, "q", (B, dims.Hq, dims.D))
+    _req(k_cache, torch.bfloat16, "k_cache")
+    _req(v_cache, torch.bfloat16, "v_cache", tuple(k_cache.shape))
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (dims.page_size, dims.G, dims.D):
+        raise ValueError("k_cache must be [n_pages][128][G][D]")
+    _req(page_table, torch.int32, "page_table", (B * dims.G, dims.topk))
+    _req(row_len, torch.int32, "row_len", (B * dims.G,))
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, dims.Hq), dtype=torch.float32, device=dev)
+    _req(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
+    _req(lse, torch.float32, "lse", (B, dims.Hq))
+    need = msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    _req(workspace, torch.uint8, "workspace")
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_sparse_attn_decode", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(row_len), B,
+          k_cache.shape[0], ctypes.byref(d), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+          _ptr(err_word), _stream(dev))
+    return out, lse
+
+
+# ------------------------------------------------------------------ whole-path helpers
+
+def dims_of(case) -> Dims:
+    """Dims of a workload from the seeded generator (msa_inputs.Case)."""
+    d = case.dims
+    return Dims(d.Hq, d.G, d.D, d.Di, d.topk, case.max_blocks, d.sm_scale, d.page)
+
+
+class DecodeStep:
+    """One MSA decode step with preallocated buffers: index scoring -> top-k ->
+    page table -> paged sparse attention.  Buffers are reused across calls so the
+    step can be replayed (and captured in a CUDA graph)."""
+
+    def __init__(self, dims: Dims, B: int, n_req: int, n_pages: int, device):
+        self.dims, self.B, self.n_req, self.n_pages = dims, B, n_req, n_pages
+        f = dict(device=device)
+        self.scores = torch.empty((B, dims.G, dims.max_blocks), dtype=torch.float32, **f)
+        self.sel = torch.empty((B, dims.G, dims.topk), dtype=torch.int32, **f)
+        self.page_table = torch.empty((B * dims.G, dims.topk), dtype=torch.int32, **f)
+        self.row_len = torch.empty((B * dims.G,), dtype=torch.int32, **f)
+        self.out = torch.empty((B, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
+        self.lse = torch.empty((B, dims.Hq), dtype=torch.float32, **f)
+        self.workspace = torch.empty((max(1, msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)),),
+                                     dtype=torch.uint8, **f)
+        self.err = new_err_word(device)
+        self.q_req = torch.arange(B, dtype=torch.int32, **f)
+        self.kernel_launches = 5   # score, top-k, page table, attention partials, merge
+
+    def scores_only(self, q_idx, kidx_cache, block_table, q_pos):
+        return msa_index_score(q_idx, kidx_cache, block_table, self.q_req, q_pos, self.dims, MSA_PHASE_DECODE,
+                               scores=self.scores, err_word=self.err)
+
+    def rest(self, q, k_cache, v_cache, block_table, q_pos, seq_lens):
+        msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
+        msa_build_page_table(self.sel, block_table, seq_lens, self.n_pages, self.dims, self.page_table,
+                             self.row_len, err_word=self.err)
+        return msa_sparse_attn_decode(q, k_cache, v_cache, self.page_table, self.row_len, self.dims, self.out,
+                                      self.lse, self.workspace, err_word=self.err)
+
+    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos):
+        self.scores_only(q_idx, kidx_cache, block_table, q_pos)
+        return self.rest(q, k_cache, v_cache, block_table, q_pos, seq_lens)
+
+
+class PrefillStep:
+    """One MSA prefill chunk: tensor-core index scoring -> top-k -> {q,blk}->{blk,q}
+    inversion -> KV-block-major sparse attention -> LSE merge."""
+
+    def __init__(self, dims: Dims, n_rows: int, n_req: int, device):
+        self.dims, self.n_rows, self.n_req = dims, n_rows, n_req
+        f = dict(device=device)
+        self.scores = torch.empty((n_rows, dims.G, dims.max_blocks), dtype=torch.float32, **f)
+        self.sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, **f)
+        n_keys = dims.G * n_req * dims.max_blocks
+        self.blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, **f)
+        self.blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, **f)
+        self.inv_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)),),
+                                  dtype=torch.uint8, **f)
+        self.o_part = torch.empty((n_rows, dims.topk, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
+        self.lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, **f)
+        self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
+        self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
+        self.err = new_err_word(device)
+        self.kernel_launches = 9   # score, top-k, 4 inversion kernels (+ memset), attention, merge
+
+    def select(self, q_idx, kidx_cache, block_table, q_req, q_pos):
+        msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
+                        scores=self.scores, err_word=self.err)
+        msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
+        msa_invert_selection(self.sel, q_req, self.n_req, self.dims, self.blk_off, self.blk_ent, self.inv_ws,
+                             err_word=self.err)
+
+    def attend(self, q, k_cache, v_cache, block_table, q_req, q_pos):
+        msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, self.blk_off, self.blk_ent,
+                                self.dims, self.o_part, self.lse_part, err_word=self.err)
+        return msa_lse_merge(self.o_part, self.lse_part, self.sel, self.dims, self.out, self.lse, err_word=self.err)
+
+    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, q_req, q_pos):
+        self.select(q_idx, kidx_cache, block_table, q_req, q_pos)
+        return self.attend(q, k_cache, v_cache, block_table, q_req, q_pos)

@@ -1,0 +1,283 @@
+// Prefill index scoring on the 5th-generation tensor cores.
+//
+// For a chunk of prefill queries the score step is a dense contraction per KV
+// group, [128 rows x Di] . [Di x 128 tokens] per KV block, followed by a block
+// max with a causal mask ("Together AI 解析如何高效服务 MiniMax M3…", sections
+// 架构/特性 and 解码索引评分内核优化: one score per 128-token block and KV group).
+//
+// One CTA owns (KV group g, 128 consecutive query rows, a chunk of up to 128
+// blocks).  Warp roles:
+//   warp 0     TMA producer: the q_idx tile once, then one k-index page per block
+//              into a 4-stage ring (128B / 64B swizzle);
+//   warp 1     TMEM owner and MMA issuer: tcgen05.mma kind::f16, M = 128 rows,
+//              N = 128 tokens, K = Di, into one of two TMEM accumulators;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = row), masked max
+//              over the 128 token columns, 32 blocks staged in shared memory and
+//              written out as coalesced 128-byte row segments.
+// All waits are bounded; a timeout raises MSA_FLAG_TIMEOUT and drains.
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kChunk = 128;            // blocks per CTA
+constexpr int kThreads = 192;
+
+template <int DI>
+struct ScoreSmem {
+    static constexpr int kTileBytes = 128 * DI * 2;
+    alignas(1024) uint8_t a[kTileBytes];
+    alignas(1024) uint8_t b[kStages][kTileBytes];
+    float sc[128][33];
+    uint64_t a_full;
+    uint64_t full[kStages], empty[kStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int jmax;
+    int req;
+    int mixed;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
+    const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+    const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req,
+    const int32_t *__restrict__ q_pos, int n_rows, int n_req, int n_pages, int G, int max_blocks,
+    int n_chunks, float *__restrict__ scores, int32_t *err) {
+    using Smem = ScoreSmem<DI>;
+    constexpr uint32_t kSw = DI == 64 ? 2u : 4u;           // descriptor swizzle: 128B / 64B
+    constexpr uint32_t kSbo = 8u * DI * 2u;                // 8 rows of DI bf16
+    constexpr uint32_t kIdesc = make_idesc_bf16(128, 128, 0, 0);
+    extern __shared__ uint8_t smem_raw[];
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int tile = blockIdx.x / n_chunks;
+    const int chunk = blockIdx.x - tile * n_chunks;
+    const int g = blockIdx.y;
+    const int row0 = tile * 128;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int j0 = chunk * kChunk;
+
+    if (tid == 0) {
+        sm.jmax = -1;
+        sm.mixed = 0;
+        sm.abort = 0;
+        sm.req = q_req[row0];
+    }
+    __syncthreads();
+    if (tid < 128 && row0 + tid < n_rows) {
+        const int p = q_pos[row0 + tid];
+        const int rq = q_req[row0 + tid];
+        if (rq != sm.req) sm.mixed = 1;
+        if (p < 0 || (p >> 7) >= max_blocks) {
+            sm.mixed = 2;
+        } else {
+            atomicMax(&sm.jmax, p >> 7);
+        }
+    }
+    __syncthreads();
+    const int req = sm.req;
+    if (sm.mixed || req < 0 || req >= n_req) {
+        if (tid == 0 && chunk == 0 && g == 0)
+            raise_flag(err, sm.mixed == 1 ? MSA_FLAG_UNSUPPORTED : MSA_FLAG_BOUNDS);
+        return;
+    }
+    const int j_end_chunk = min(j0 + kChunk, max_blocks);
+    const int j1 = min(j_end_chunk, sm.jmax + 1);       // blocks [j0, j1) hold candidates
+    const int nblk = j1 - j0;
+
+    // rows of this tile; blocks past every row's own block are -inf
+    auto fill_neg_inf = [&](int from, int to) {
+        if (from >= to || tid < 64) return;
+        const int e = tid - 64;                          // 128 epilogue threads
+        for (int i = 0; i < 128; ++i) {
+            const int grow = row0 + i;
+            if (grow >= n_rows) break;
+            float *o = scores + (size_t(grow) * G + g) * max_blocks;
+            for (int j = from + e; j < to; j += 128) o[j] = -INFINITY;
+        }
+    };
+    if (nblk <= 0) {
+        fill_neg_inf(j0, j_end_chunk);
+        return;
+    }
+
+    if (tid == 0) {
+        mbar_init(&sm.a_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.acc_full[a], 1);
+            mbar_init(&sm.acc_empty[a], 4);
+        }
+        mbar_init(&sm.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&amap);
+            tma_prefetch_desc(&bmap);
+            mbar_arrive_expect_tx(&sm.a_full, Smem::kTileBytes);
+            tma_load_3d(sm.a, &amap, &sm.a_full, 0, g, row0);
+            int issued = 0;
+            for (int jj = 0; jj < nblk; ++jj) {
+                const int s = jj % kStages;
+                if (jj >= kStages && !mbar_wait(&sm.empty[s], ((jj / kStages) - 1) & 1, err, &sm.abort)) break;
+                int page = block_table[size_t(req) * max_blocks + j0 + jj];
+                if (page < 0 || page >= n_pages) {
+                    raise_flag(err, MSA_FLAG_BOUNDS);
+                    page = 0;
+                }
+                mbar_arrive_expect_tx(&sm.full[s], Smem::kTileBytes);
+                tma_load_4d(sm.b[s], &bmap, &sm.full[s], 0, g, 0, page);
+                issued = jj + 1;
+            }
+            // on abort: let every issued copy land before the CTA can exit
+            if (sm.abort) {
+                for (int jj = max(0, issued - kStages); jj < issued; ++jj)
+                    mbar_wait(&sm.full[jj % kStages], (jj / kStages) & 1, err, nullptr);
+                mbar_wait(&sm.a_full, 0, err, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t a_addr = smem_u32(sm.a);
+            bool ok = mbar_wait(&sm.a_full, 0, err, &sm.abort);
+            for (int jj = 0; ok && jj < nblk; ++jj) {
+                const int s = jj % kStages;
+                const int acc = jj & 1;
+                if (!mbar_wait(&sm.full[s], (jj / kStages) & 1, err, &sm.abort)) break;
+                if (jj >= 2 && !mbar_wait(&sm.acc_empty[acc], ((jj >> 1) - 1) & 1, err, &sm.abort)) break;
+                tc_fence_after();
+                const uint32_t b_addr = smem_u32(sm.b[s]);
+#pragma unroll
+                for (int k = 0; k < DI / 16; ++k) {
+                    const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, kSbo, kSw);
+                    const uint64_t bd = make_smem_desc(b_addr + k * 32, 16, kSbo, kSw);
+                    mma_bf16(tmem + uint32_t(acc * 128), ad, bd, kIdesc, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&sm.empty[s]);
+                mma_commit(&sm.acc_full[acc]);
+            }
+            // all issued MMAs complete before TMEM can be released
+            mma_commit(&sm.drain);
+            mbar_wait(&sm.drain, 0, err, nullptr);
+        }
+    } else {
+        // epilogue: thread = accumulator row (TMEM lane quadrant = warp % 4)
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int grow = row0 + row;
+        const int p = grow < n_rows ? q_pos[grow] : -1;
+        const int ew = warp - 2;
+        const uint32_t lane_addr = tmem + (uint32_t(quad * 32) << 16);
+        int jj = 0;
+        for (; jj < nblk; ++jj) {
+            const int acc = jj & 1;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full[acc], (jj >> 1) & 1, err, &sm.abort));
+            if (!ok) break;
+            tc_fence_after();
+            const int lim = p - (j0 + jj) * 128;     // columns c <= lim are visible
+            float best = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(lane_addr + uint32_t(acc * 128 + c0), v);
+                tmem_ld_wait();
+                if (lim >= c0 + 31) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) best = fmaxf(best, __uint_as_float(v[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        best = fmaxf(best, (c0 + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+            sm.sc[row][jj & 31] = best;
+            if ((jj & 31) == 31 || jj == nblk - 1) {
+                epi_bar();
+                const int base = jj & ~31;
+                const int ncols = jj - base + 1;
+                for (int i = 0; i < 32; ++i) {
+                    const int r = ew * 32 + i;
+                    const int gr = row0 + r;
+                    if (gr < n_rows && lane < ncols)
+                        scores[(size_t(gr) * G + g) * max_blocks + j0 + base + lane] = sm.sc[r][lane];
+                }
+                epi_bar();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    fill_neg_inf(j1, j_end_chunk);
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+template <int DI>
+cudaError_t launch_di(const void *q_idx, const void *kidx, const int32_t *bt, const int32_t *q_req,
+                      const int32_t *q_pos, int n_rows, int n_req, int n_pages, const Shape &s, float *scores,
+                      int32_t *err, cudaStream_t st) {
+    alignas(64) CUtensorMap am, bm;
+    const char *why = nullptr;
+    {
+        const uint64_t dims[3] = {uint64_t(DI), uint64_t(s.G), uint64_t(n_rows)};
+        const uint64_t strides[2] = {uint64_t(DI) * 2, uint64_t(s.G) * DI * 2};
+        const uint32_t box[3] = {uint32_t(DI), 1u, 128u};
+        if (!encode_tensor_map(&am, 3, q_idx, dims, strides, box, DI * 2, &why)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[4] = {uint64_t(DI), uint64_t(s.G), 128ull, uint64_t(n_pages)};
+        const uint64_t strides[3] = {uint64_t(DI) * 2, uint64_t(s.G) * DI * 2, 128ull * s.G * DI * 2};
+        const uint32_t box[4] = {uint32_t(DI), 1u, 128u, 1u};
+        if (!encode_tensor_map(&bm, 4, kidx, dims, strides, box, DI * 2, &why)) return cudaErrorInvalidValue;
+    }
+    const int n_tiles = (n_rows + 127) / 128;
+    const int n_chunks = (s.max_blocks + kChunk - 1) / kChunk;
+    const size_t smem = sizeof(ScoreSmem<DI>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_score_prefill<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    const long long gx = 1LL * n_tiles * n_chunks;
+    if (gx > 0x7fffffffLL || s.G > 65535) return cudaErrorInvalidConfiguration;
+    dim3 grid(unsigned(gx), unsigned(s.G));
+    k_score_prefill<DI><<<grid, kThreads, smem, st>>>(am, bm, bt, q_req, q_pos, n_rows, n_req, n_pages, s.G,
+                                                      s.max_blocks, n_chunks, scores, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                 const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
+                                 int n_pages, const Shape &s, float *scores, int32_t *err, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    if (s.Di == 64)
+        return launch_di<64>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores, err, st);
+    if (s.Di == 32)
+        return launch_di<32>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores, err, st);
+    return cudaErrorNotSupported;
+}
+
+}  // namespace msa

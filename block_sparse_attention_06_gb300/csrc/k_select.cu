@@ -1,0 +1,364 @@
+// Selection bookkeeping: top-k blocks per (row, group), decode page tables and
+// the {q, kv block} -> {kv block, q} inversion.
+//
+// "Together AI 解析如何高效服务 MiniMax M3…": 架构/特性 (the K most relevant blocks
+// per KV group), 将 MSA 与分页注意力集成 (page tables per flattened (request,
+// group) row), KV 块主序稀疏注意力 (the mapping is reorganised from {q, kv block}
+// to {kv block, q}), 未来工作 (top-k and the remap are small kernels of their own).
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+// ------------------------------------------------------------------ top-k
+
+// Sort key: higher score first, lower block id on ties; -0.0 == +0.0.  Every
+// candidate key is non-zero (the low word is ~j with j < 2^31), so 0 marks "none".
+__device__ __forceinline__ uint64_t block_key(float s, int j, int32_t *err) {
+    if (s != s) {
+        raise_flag(err, MSA_FLAG_NAN);
+        s = -INFINITY;
+    }
+    const uint32_t u = __float_as_uint(s == 0.0f ? 0.0f : s);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (uint64_t(ord) << 32) | uint64_t(~uint32_t(j));
+}
+
+__device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// One warp per (row, group); keys of candidates j = lane + 32 * i live in registers.
+template <int PER>
+__global__ void __launch_bounds__(256) k_topk_warp(const float *__restrict__ scores,
+                                                   const int32_t *__restrict__ q_pos, int n_rows,
+                                                   int G, int max_blocks, int topk,
+                                                   int32_t *__restrict__ sel, int32_t *err) {
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (item >= n_rows * G) return;
+    const int r = item / G;
+    int32_t *out = sel + size_t(item) * topk;
+    const int p = q_pos[r];
+    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= 32 * PER) {
+        for (int i = lane; i < topk; i += 32) out[i] = -1;
+        if (lane == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const float *s = scores + size_t(item) * max_blocks;
+    uint64_t keys[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = lane + 32 * i;
+        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+    }
+    int mine = 0x7fffffff;
+    uint64_t prev = ~0ull;
+    for (int round = 0; round < k_eff - 1; ++round) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const uint64_t k = keys[i];
+            best = (k < prev && k > best) ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
+        prev = best;
+        if (lane == round) mine = int(~uint32_t(best));
+    }
+    int rank = 0;
+    for (int l = 0; l < k_eff - 1; ++l) {
+        const int other = __shfl_sync(0xffffffffu, mine, l);
+        rank += other < mine ? 1 : 0;
+    }
+    if (lane < k_eff - 1) out[rank] = mine;
+    if (lane == 0) out[k_eff - 1] = own;
+    for (int i = k_eff + lane; i < topk; i += 32) out[i] = -1;
+}
+
+// One CTA of NT threads per (row, group) for long contexts.
+template <int NT, int PER>
+__global__ void __launch_bounds__(NT) k_topk_cta(const float *__restrict__ scores,
+                                                 const int32_t *__restrict__ q_pos, int G,
+                                                 int max_blocks, int topk, int32_t *__restrict__ sel,
+                                                 int32_t *err) {
+    constexpr int NW = NT / 32;
+    __shared__ uint64_t wbest[NW];
+    __shared__ int picked[32];
+    const int item = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = item / G;
+    int32_t *out = sel + size_t(item) * topk;
+    const int p = q_pos[r];
+    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= NT * PER) {
+        for (int i = tid; i < topk; i += NT) out[i] = -1;
+        if (tid == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const float *s = scores + size_t(item) * max_blocks;
+    uint64_t keys[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = tid + NT * i;
+        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+    }
+    uint64_t prev = ~0ull;
+    for (int round = 0; round < k_eff - 1; ++round) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const uint64_t k = keys[i];
+            best = (k < prev && k > best) ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
+        if (lane == 0) wbest[warp] = best;
+        __syncthreads();
+        best = 0;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) best = max_u64(best, wbest[w]);
+        __syncthreads();
+        prev = best;
+        if (tid == 0) picked[round] = int(~uint32_t(best));
+    }
+    if (tid == 0) {
+        const int n = k_eff - 1;
+        for (int a = 1; a < n; ++a) {
+            const int v = picked[a];
+            int b = a - 1;
+            while (b >= 0 && picked[b] > v) {
+                picked[b + 1] = picked[b];
+                --b;
+            }
+            picked[b + 1] = v;
+        }
+        for (int i = 0; i < n; ++i) out[i] = picked[i];
+        out[n] = own;
+    }
+    for (int i = k_eff + tid; i < topk; i += NT) out[i] = -1;
+}
+
+// ------------------------------------------------------------------ decode page table
+
+__global__ void k_page_table(const int32_t *__restrict__ sel, const int32_t *__restrict__ block_table,
+                             const int32_t *__restrict__ seq_lens, int B, int G, int topk,
+                             int max_blocks, int n_pages, int32_t *__restrict__ pt,
+                             int32_t *__restrict__ row_len, int32_t *err) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= B * G) return;
+    const int b = r / G;
+    const int L = seq_lens[b];
+    int len = 0;
+    for (int s = 0; s < topk; ++s) {
+        const int j = sel[size_t(r) * topk + s];
+        int page = -1;
+        if (j >= 0) {
+            if (j >= max_blocks) {
+                raise_flag(err, MSA_FLAG_BOUNDS);
+            } else {
+                page = block_table[size_t(b) * max_blocks + j];
+                if (page < 0 || page >= n_pages) {
+                    raise_flag(err, MSA_FLAG_BOUNDS);
+                    page = -1;
+                } else {
+                    len += max(0, min(128, L - j * 128));
+                }
+            }
+        }
+        pt[size_t(r) * topk + s] = page;
+    }
+    row_len[r] = len;
+}
+
+// ------------------------------------------------------------------ inversion
+//
+// Stable counting sort through a per-key bitmap over query rows: mark bits with
+// atomicOr (order-free), count per key, scan, then emit each key's rows in
+// ascending order.  Deterministic for any schedule.
+
+struct InvLayout {
+    size_t n_keys, words, bitmap_off, cnt_off, bytes;
+};
+
+__host__ __device__ inline InvLayout inv_layout(int n_rows, int n_req, int G, int max_blocks) {
+    InvLayout l;
+    l.n_keys = size_t(G) * n_req * max_blocks;
+    l.words = (size_t(n_rows) + 31) / 32;
+    l.bitmap_off = 0;
+    size_t bm = l.n_keys * l.words * 4;
+    l.cnt_off = (bm + 255) & ~size_t(255);
+    l.bytes = l.cnt_off + ((l.n_keys * 4 + 255) & ~size_t(255));
+    return l;
+}
+
+__global__ void k_inv_mark(const int32_t *__restrict__ sel, const int32_t *__restrict__ q_req, int n_rows,
+                           int n_req, int G, int topk, int max_blocks, uint32_t *__restrict__ bitmap,
+                           size_t words, int32_t *err) {
+    const size_t e = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= size_t(n_rows) * G * topk) return;
+    const int j = sel[e];
+    if (j < 0) return;
+    const int q = int(e / (size_t(G) * topk));
+    const int g = int((e / topk) % G);
+    const int req = q_req[q];
+    if (j >= max_blocks || req < 0 || req >= n_req) {
+        raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const size_t key = (size_t(g) * n_req + req) * max_blocks + j;
+    const uint32_t bit = 1u << (q & 31);
+    const uint32_t old = atomicOr(bitmap + key * words + (q >> 5), bit);
+    if (old & bit) raise_flag(err, MSA_FLAG_BOUNDS);   // a block listed twice for one (row, group)
+}
+
+__global__ void k_inv_count(const uint32_t *__restrict__ bitmap, size_t words, size_t n_keys,
+                            int32_t *__restrict__ cnt) {
+    const size_t key = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (key >= n_keys) return;
+    const uint32_t *row = bitmap + key * words;
+    int c = 0;
+    for (size_t w = lane; w < words; w += 32) c += __popc(row[w]);
+    c = warp_sum_i(c);
+    if (lane == 0) cnt[key] = c;
+}
+
+// Exclusive scan of n counts into off[0..n] with one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) k_inv_scan(const int32_t *__restrict__ cnt, size_t n,
+                                                   int32_t *__restrict__ off) {
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t carry_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (size_t base = 0; base < n; base += 1024) {
+        const size_t i = base + tid;
+        const int32_t v = i < n ? cnt[i] : 0;
+        int32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;   // inclusive over warps
+        }
+        __syncthreads();
+        const int32_t carry = carry_s;
+        const int32_t excl = carry + (warp ? wsum[warp - 1] : 0) + x - v;
+        if (i < n) off[i] = excl;
+        __syncthreads();
+        if (tid == 1023) carry_s = excl + v;
+        __syncthreads();
+    }
+    if (tid == 0) off[n] = carry_s;
+}
+
+__global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, size_t words, size_t n_keys,
+                           const int32_t *__restrict__ off, const int32_t *__restrict__ sel, int n_req,
+                           int G, int topk, int max_blocks, int32_t *__restrict__ ent) {
+    const size_t key = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (key >= n_keys) return;
+    const int g = int(key / (size_t(n_req) * max_blocks));
+    const int j = int(key % size_t(max_blocks));
+    const uint32_t *row = bitmap + key * words;
+    int32_t base = off[key];
+    for (size_t w0 = 0; w0 < words; w0 += 32) {
+        const uint32_t word = (w0 + lane < words) ? row[w0 + lane] : 0u;
+        const int c = __popc(word);
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        int pos = base + x - c;
+        uint32_t bits = word;
+        while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int q = int((w0 + lane) * 32 + b);
+            const int32_t *sq = sel + (size_t(q) * G + g) * topk;
+            int slot = 0;
+            for (int s = 0; s < topk; ++s)
+                if (sq[s] == j) slot = s;
+            ent[pos++] = q * topk + slot;
+        }
+        base += __shfl_sync(0xffffffffu, x, 31);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, const Shape &s,
+                        int32_t *sel, int32_t *err, cudaStream_t st) {
+    const int items = n_rows * s.G;
+    if (items <= 0) return cudaSuccess;
+    const int mb = s.max_blocks;
+    if (mb <= 1024) {
+        const unsigned grid = unsigned((items + 7) / 8);
+        if (mb <= 128)
+            k_topk_warp<4><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
+        else if (mb <= 512)
+            k_topk_warp<16><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
+        else
+            k_topk_warp<32><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
+    } else if (mb <= 8192) {
+        k_topk_cta<256, 32><<<unsigned(items), 256, 0, st>>>(scores, q_pos, s.G, mb, s.topk, sel, err);
+    } else if (mb <= 16384) {
+        k_topk_cta<512, 32><<<unsigned(items), 512, 0, st>>>(scores, q_pos, s.G, mb, s.topk, sel, err);
+    } else {
+        return cudaErrorNotSupported;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_page_table(const int32_t *sel, const int32_t *block_table, const int32_t *seq_lens,
+                              int B, int n_pages, const Shape &s, int32_t *pt, int32_t *row_len,
+                              int32_t *err, cudaStream_t st) {
+    const int rows = B * s.G;
+    if (rows <= 0) return cudaSuccess;
+    k_page_table<<<unsigned((rows + 127) / 128), 128, 0, st>>>(sel, block_table, seq_lens, B, s.G, s.topk,
+                                                                s.max_blocks, n_pages, pt, row_len, err);
+    return cudaGetLastError();
+}
+
+size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s) {
+    return inv_layout(n_rows, n_req, s.G, s.max_blocks).bytes;
+}
+
+cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
+                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, void *ws,
+                          int32_t *err, cudaStream_t st) {
+    const InvLayout l = inv_layout(n_rows, n_req, s.G, s.max_blocks);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(w + l.bitmap_off);
+    int32_t *cnt = reinterpret_cast<int32_t *>(w + l.cnt_off);
+    cudaError_t e = cudaMemsetAsync(bitmap, 0, l.n_keys * l.words * 4, st);
+    if (e != cudaSuccess) return e;
+    const size_t n_ent = size_t(n_rows) * s.G * s.topk;
+    if (n_ent > 0) {
+        k_inv_mark<<<unsigned((n_ent + 255) / 256), 256, 0, st>>>(sel, q_req, n_rows, n_req, s.G, s.topk,
+                                                                   s.max_blocks, bitmap, l.words, err);
+    }
+    const unsigned kgrid = unsigned((l.n_keys + 7) / 8);
+    k_inv_count<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, cnt);
+    k_inv_scan<<<1, 1024, 0, st>>>(cnt, l.n_keys, blk_off);
+    k_inv_emit<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, blk_off, sel, n_req, s.G, s.topk,
+                                      s.max_blocks, blk_ent);
+    return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,63 @@
+// Host-side launchers shared between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "msa.h"
+
+namespace msa {
+
+struct Shape {
+    int Hq, G, D, Di, topk, max_blocks, hpg;
+    float sm_scale;
+};
+
+cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
+                                int n_pages, const Shape &s, float *scores, int32_t *err,
+                                cudaStream_t st);
+
+cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                 const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
+                                 int n_pages, const Shape &s, float *scores, int32_t *err,
+                                 cudaStream_t st);
+
+cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, const Shape &s,
+                        int32_t *sel, int32_t *err, cudaStream_t st);
+
+cudaError_t launch_page_table(const int32_t *sel, const int32_t *block_table, const int32_t *seq_lens,
+                              int B, int n_pages, const Shape &s, int32_t *pt, int32_t *row_len,
+                              int32_t *err, cudaStream_t st);
+
+size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s);
+cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
+                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, void *ws,
+                          int32_t *err, cudaStream_t st);
+
+cudaError_t launch_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_table, const int32_t *q_req,
+                                const int32_t *q_pos, const int32_t *blk_off,
+                                const int32_t *blk_ent, int n_rows, int n_req, int n_pages,
+                                const Shape &s, void *o_part, float *lse_part, int32_t *err,
+                                cudaStream_t st);
+
+cudaError_t launch_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel,
+                             int n_rows, const Shape &s, void *out, float *lse, int32_t *err,
+                             cudaStream_t st);
+
+size_t decode_workspace_bytes(int B, const Shape &s);
+cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *pt, const int32_t *row_len, int B, int n_pages,
+                               const Shape &s, void *out, float *lse, void *ws, int32_t *err,
+                               cudaStream_t st);
+
+// Tensor-map creation through the driver entry point (no libcuda link dependency).
+bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *dims,
+                       const uint64_t *strides_bytes, const uint32_t *box, int swizzle_bytes,
+                       const char **why);
+
+int sm_count();
+
+}  // namespace msa

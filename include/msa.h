@@ -1,0 +1,254 @@
+/*
+ * msa.h -- C ABI of libmsa.so, the MiniMax Sparse Attention (MSA) hot path on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [T-zh]  "Together AI 解析如何高效服务 MiniMax M3：1M token 上下文与多模态推理优化"
+ *           (aihot.news) -- sections 架构/特性 (two-part MSA), KV 块主序稀疏注意力
+ *           (block-major prefill + Log-Sum-Exp reduction), 将 MSA 与分页注意力集成
+ *           (decode page tables, groups flattened into the batch), 解码索引评分内核优化
+ *           (decode index scoring), 未来工作 (top-k / remap kernels).
+ *   [T-ja]  "MiniMax-M3の効率的な推論サービス：100万トークンコンテキストとマルチモーダルを後悔なく実現"
+ *           (news.chathome.org) -- the same material in summary.
+ *   [NV-ja] "NVIDIA 加速インフラ上で MiniMax M3 を活用した長文脈推論とエージェントワークフローの展開"
+ *           (news.ainew.jp) -- MSA paragraph after Table 1 (each KV block read once).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no memory.  bf16 tensors are passed as `const void *` and hold
+ *     IEEE bfloat16 bit patterns.  All tensors are dense, row-major, with the
+ *     shapes written beside each argument.
+ *   - Paged caches share one page pool of n_pages pages of page_size = 128
+ *     tokens, token stride = G * width (the strided KV view of [T-zh
+ *     将 MSA 与分页注意力集成]):  k_cache, v_cache bf16 [n_pages][128][G][D],
+ *     kidx_cache bf16 [n_pages][128][G][Di] (same page ids as K/V).
+ *   - block_table int32 [n_req][dims->max_blocks]: logical block -> page.
+ *   - A query row has an absolute position q_pos and a request q_req.  Its
+ *     candidate blocks are 0 .. q_pos/128; block q_pos/128 is its own block.
+ *     Query head h belongs to KV group h / (Hq / G).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream); calls return after host-side validation, never synchronise,
+ *     and never throw.
+ *   - Host-side validation failures return MSA_ERR_INVALID_ARG or
+ *     MSA_ERR_UNSUPPORTED before anything is enqueued.  Errors the kernels
+ *     detect (an out-of-range page or block id, a malformed selection, a wait
+ *     that timed out) are OR-ed as flags into *err_word, a caller-owned device
+ *     int32; the affected outputs are then unspecified.  msa_check() reads
+ *     and clears that word.
+ *   - Supported shapes: page_size == 128, Hq % G == 0, Hq / G in {4, 8},
+ *     D in {64, 128}, Di in {32, 64}, 1 <= topk <= 32.  Others return
+ *     MSA_ERR_UNSUPPORTED.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent dims     */
+    MSA_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set                  */
+    MSA_ERR_CUDA = 3,          /* a CUDA runtime call failed (see msa_last_error)    */
+    MSA_ERR_DEVICE_BOUNDS = 4, /* a kernel met an out-of-range index (err_word)      */
+    MSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait expired (err_word)      */
+    MSA_ERR_WORKSPACE = 6,     /* workspace smaller than msa_workspace_bytes()       */
+    MSA_ERR_DEVICE_UNSUPPORTED = 7 /* a kernel met a layout it cannot handle (err_word) */
+} msa_status_t;
+
+/* Bits of the device error word. */
+#define MSA_FLAG_BOUNDS      0x1
+#define MSA_FLAG_TIMEOUT     0x2
+#define MSA_FLAG_UNSUPPORTED 0x4
+#define MSA_FLAG_NAN         0x8
+
+typedef struct {
+    int32_t Hq;         /* query heads                                          */
+    int32_t G;          /* KV groups (= KV heads)                               */
+    int32_t D;          /* head dim of Q/K/V                                    */
+    int32_t Di;         /* index-key dim (one index head per KV group)          */
+    int32_t page_size;  /* tokens per page = per KV block; must be 128          */
+    int32_t topk;       /* blocks kept per (row, group), own block included     */
+    int32_t max_blocks; /* block_table row stride = last dim of the scores      */
+    float sm_scale;     /* attention logit scale, normally 1/sqrt(D)            */
+} msa_dims_t;
+
+typedef void *msa_stream_t;
+
+/* Phase selector of msa_index_score. */
+#define MSA_PHASE_DECODE  0
+#define MSA_PHASE_PREFILL 1
+
+/* Operation selector of msa_workspace_bytes. */
+#define MSA_OP_INVERT 0
+#define MSA_OP_DECODE 1
+
+/*
+ * msa_index_score -- block scores for every (row, group, candidate block).
+ * [T-zh 解码索引评分内核优化]: the query-side index vector is compared with every
+ * candidate key-side index vector and each 128-token KV block is reduced to one
+ * score; one score per KV group ([T-zh 架构/特性]).  The reduction is the MAX of
+ * the raw dot products over the block's tokens at positions <= q_pos.
+ *
+ *   q_idx       bf16 [n_rows][G][Di]
+ *   kidx_cache  bf16 [n_pages][128][G][Di]
+ *   block_table int32 [n_req][max_blocks]
+ *   q_req, q_pos int32 [n_rows]
+ *   scores      fp32 [n_rows][G][max_blocks]  out; -inf for blocks > q_pos/128
+ *   phase       MSA_PHASE_DECODE: each row streams its own candidate pages
+ *               (HBM-bound path, any rows).  MSA_PHASE_PREFILL: rows are
+ *               scored 128 at a time on the tensor cores; every run of 128
+ *               consecutive rows (the last may be shorter) must belong to one
+ *               request, otherwise MSA_FLAG_UNSUPPORTED is raised.
+ * A page id outside [0, n_pages) or a q_pos/128 >= max_blocks raises
+ * MSA_FLAG_BOUNDS.
+ */
+msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
+                             const int32_t *q_req, const int32_t *q_pos, int32_t n_rows,
+                             int32_t n_req, int32_t n_pages, const msa_dims_t *dims, int32_t phase,
+                             float *scores, int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_topk_blocks -- per (row, group): the own block q_pos/128 is always kept;
+ * the other candidates 0 .. q_pos/128 - 1 are ranked by (score descending,
+ * block id ascending) and the best k_eff - 1 are kept, k_eff = min(topk,
+ * q_pos/128 + 1).  [T-zh 架构/特性]: the K most relevant blocks per KV group;
+ * [T-zh 解码索引评分内核优化]: only the top blocks go to attention.  -0.0 ranks
+ * equal to +0.0; a NaN score raises MSA_FLAG_NAN and ranks as -inf.
+ *
+ *   scores fp32 [n_rows][G][max_blocks]
+ *   q_pos  int32 [n_rows]
+ *   sel    int32 [n_rows][G][topk]  out; ascending block ids, -1 padding
+ * Candidate counts up to 32768 blocks (4M tokens) are supported.
+ */
+msa_status_t msa_topk_blocks(const float *scores, const int32_t *q_pos, int32_t n_rows,
+                             const msa_dims_t *dims, int32_t *sel, int32_t *err_word,
+                             msa_stream_t stream);
+
+/*
+ * msa_build_page_table -- decode page tables.  [T-zh 将 MSA 与分页注意力集成]: a page
+ * table is built from the selected blocks and the KV-group dimension is
+ * flattened into the batch, so row r = b * G + g has its own table.
+ *
+ *   sel         int32 [B][G][topk]   decode selection (row b at seq_lens[b] - 1)
+ *   block_table int32 [B][max_blocks]
+ *   seq_lens    int32 [B]            cached tokens incl. the new one
+ *   page_table  int32 [B*G][topk]    out; physical page per slot, -1 padding
+ *   row_len     int32 [B*G]          out; tokens the row attends (selected
+ *                                    blocks clipped at seq_lens[b])
+ */
+msa_status_t msa_build_page_table(const int32_t *sel, const int32_t *block_table,
+                                  const int32_t *seq_lens, int32_t B, int32_t n_pages,
+                                  const msa_dims_t *dims, int32_t *page_table, int32_t *row_len,
+                                  int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_invert_selection -- {q, kv block} -> {kv block, q}.  [T-zh KV 块主序稀疏注意力]:
+ * the mapping is reorganised so attention can loop over KV blocks outside and
+ * queries inside.  Keys are key = (g * n_req + q_req[q]) * max_blocks + block;
+ * the output is a CSR whose entries are q * topk + slot, ascending in q inside
+ * each key (deterministic, a stable counting sort).
+ *
+ *   sel      int32 [n_rows][G][topk]
+ *   q_req    int32 [n_rows]
+ *   blk_off  int32 [G * n_req * max_blocks + 1]  out
+ *   blk_ent  int32 [n_rows * G * topk]           out (first blk_off[last] used)
+ *   workspace device scratch of msa_workspace_bytes(MSA_OP_INVERT, ...) bytes
+ */
+msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int32_t n_rows,
+                                  int32_t n_req, const msa_dims_t *dims, int32_t *blk_off,
+                                  int32_t *blk_ent, void *workspace, size_t workspace_bytes,
+                                  int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_sparse_attn_prefill -- KV-block-major sparse attention.  [T-zh KV 块主序稀疏注意力]
+ * and [T-ja, KV block-major kernel paragraph]: for each (group, KV block) the
+ * block's K and V are read once and every query that selected it attends it;
+ * [NV-ja]: each KV cache block is read once with contiguous access.  For each
+ * CSR entry (q, slot) of key (g, req, j) and each head h of group g, writes the
+ * softmax-normalised partial output over block j's tokens at positions <=
+ * q_pos[q], and its log-sum-exp (natural log of the sum of exp of the
+ * sm_scale-scaled logits).  Slots without an entry are not written.
+ *
+ *   q        bf16 [n_rows][Hq][D]
+ *   k_cache, v_cache bf16 [n_pages][128][G][D]
+ *   block_table int32 [n_req][max_blocks];  q_req, q_pos int32 [n_rows]
+ *   blk_off, blk_ent  the CSR of msa_invert_selection (same n_req, dims)
+ *   o_part   bf16 [n_rows][topk][Hq][D]  out
+ *   lse_part fp32 [n_rows][topk][Hq]     out
+ */
+msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_table, const int32_t *q_req,
+                                     const int32_t *q_pos, const int32_t *blk_off,
+                                     const int32_t *blk_ent, int32_t n_rows, int32_t n_req,
+                                     int32_t n_pages, const msa_dims_t *dims, void *o_part,
+                                     float *lse_part, int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_lse_merge -- Log-Sum-Exp reduction of per-block partials.  [T-zh KV
+ * 块主序稀疏注意力]: the partial O of each KV block is rescaled and summed.  For
+ * each (q, h) over the slots s with sel[q][h / (Hq/G)][s] >= 0:
+ *   lse = m + log(sum_s exp(lse_s - m)),  m = max_s lse_s
+ *   out = sum_s exp(lse_s - lse) * O_s
+ * Slots with sel < 0 are never read.
+ *
+ *   o_part   bf16 [n_rows][topk][Hq][D];  lse_part fp32 [n_rows][topk][Hq]
+ *   sel      int32 [n_rows][G][topk]
+ *   out      bf16 [n_rows][Hq][D]  out;  lse fp32 [n_rows][Hq]  out
+ */
+msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel,
+                           int32_t n_rows, const msa_dims_t *dims, void *out, float *lse,
+                           int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_sparse_attn_decode -- decode attention over per-(request, group) page
+ * tables ([T-zh 将 MSA 与分页注意力集成]): row r = b * G + g reads its row_len[r]
+ * tokens from pages page_table[r][0], [1], ... in order (slot s holds tokens
+ * s*128 .. s*128+127 of the row); the Hq/G heads of group g attend them.
+ * Split by page: one partial per (row, slot) in the workspace, then an LSE
+ * merge (the same reduction as msa_lse_merge).
+ *
+ *   q          bf16 [B][Hq][D]
+ *   page_table int32 [B*G][topk];  row_len int32 [B*G]
+ *   out        bf16 [B][Hq][D]  out;  lse fp32 [B][Hq]  out
+ *   workspace  device scratch of msa_workspace_bytes(MSA_OP_DECODE, B, ...) bytes
+ */
+msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *page_table, const int32_t *row_len, int32_t B,
+                                    int32_t n_pages, const msa_dims_t *dims, void *out, float *lse,
+                                    void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                    msa_stream_t stream);
+
+/*
+ * msa_workspace_bytes -- device scratch needed by an operation:
+ *   MSA_OP_INVERT: n_rows query rows, n_req requests;
+ *   MSA_OP_DECODE: n_rows = B decode requests (n_req ignored).
+ * Returns 0 for invalid arguments.
+ */
+size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_dims_t *dims);
+
+/*
+ * msa_check -- synchronise `stream`, read the device error word, reset it to 0,
+ * and map it to a status (MSA_OK when no flag is set; bounds before NaN before
+ * timeout before unsupported).
+ */
+msa_status_t msa_check(int32_t *err_word, msa_stream_t stream);
+
+/* Human-readable name of a status. */
+const char *msa_status_str(msa_status_t status);
+
+/* Detail of the last MSA_ERR_* returned on this thread (static storage). */
+const char *msa_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

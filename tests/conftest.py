@@ -8,6 +8,23 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def build_library():
+    """Build libmsa.so (no-op when up to date) and the oracle; the package import needs the library."""
+    import importlib.util
+    path = os.path.join(ROOT, "block_sparse_attention_06_gb300", "_build.py")
+    spec = importlib.util.spec_from_file_location("msa_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    lib = mod.build()
+    import oracle
+    oracle.build()
+    return lib
+
+
+def pytest_sessionstart(session):
+    build_library()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
 

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/msa.h declares, and rejects bad arguments on the host (status codes)
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tests.conftest import build_library
+    return ctypes.CDLL(build_library())
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(msa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("msa_index_score", "msa_topk_blocks", "msa_build_page_table", "msa_invert_selection",
+              "msa_sparse_attn_prefill", "msa_lse_merge", "msa_sparse_attn_decode", "msa_workspace_bytes",
+              "msa_check", "msa_status_str", "msa_last_error", "msa_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libmsa.so does not export {n}"
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("Hq", ctypes.c_int32), ("G", ctypes.c_int32), ("D", ctypes.c_int32), ("Di", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("topk", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float)]
+
+
+def good_dims(**kw):
+    d = dict(Hq=64, G=8, D=128, Di=64, page_size=128, topk=16, max_blocks=469, sm_scale=0.088)
+    d.update(kw)
+    return Dims(**d)
+
+
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+
+
+def test_status_strings(lib):
+    lib.msa_status_str.restype = ctypes.c_char_p
+    assert lib.msa_status_str(0) == b"MSA_OK"
+    assert lib.msa_status_str(6) == b"MSA_ERR_WORKSPACE"
+    lib.msa_version.restype = ctypes.c_int32
+    assert lib.msa_version() >= 100
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(page_size=64), 2), (dict(topk=33), 2), (dict(topk=0), 1), (dict(Hq=63), 1),
+    (dict(Di=48), 2), (dict(G=3, Hq=24), 2), (dict(max_blocks=0), 1),
+])
+def test_index_score_rejects_bad_dims(lib, kw, status):
+    d = good_dims(**kw)
+    rc = lib.msa_index_score(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 8, 100, ctypes.byref(d), 0, FAKE, FAKE, None)
+    assert rc == status
+    lib.msa_last_error.restype = ctypes.c_char_p
+    assert lib.msa_last_error()
+
+
+def test_null_pointers_and_bad_sizes(lib):
+    d = good_dims()
+    assert lib.msa_index_score(None, FAKE, FAKE, FAKE, FAKE, 8, 8, 100, ctypes.byref(d), 0, FAKE, FAKE, None) == 1
+    assert lib.msa_index_score(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 8, 100, ctypes.byref(d), 7, FAKE, FAKE, None) == 1
+    assert lib.msa_topk_blocks(FAKE, None, 4, ctypes.byref(d), FAKE, FAKE, None) == 1
+    assert lib.msa_topk_blocks(FAKE, FAKE, -1, ctypes.byref(d), FAKE, FAKE, None) == 1
+    assert lib.msa_build_page_table(FAKE, FAKE, FAKE, 2, 0, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
+    assert lib.msa_lse_merge(FAKE, FAKE, None, 4, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
+    assert lib.msa_check(None, None) == 1
+    # empty work is a no-op that never touches the device
+    assert lib.msa_topk_blocks(None, None, 0, ctypes.byref(d), None, None, None) == 0
+    assert lib.msa_sparse_attn_decode(None, None, None, None, None, 0, 10, ctypes.byref(d), None, None, None, 0,
+                                      None, None) == 0
+
+
+def test_attention_shape_limits(lib):
+    for kw in (dict(Hq=16, G=8), dict(D=96), dict(sm_scale=0.0)):
+        d = good_dims(**kw)
+        rc = lib.msa_sparse_attn_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 100,
+                                         ctypes.byref(d), FAKE, FAKE, FAKE, None)
+        assert rc in (1, 2), kw
+
+
+def test_workspace_sizes_and_errors(lib):
+    lib.msa_workspace_bytes.restype = ctypes.c_size_t
+    d = good_dims(max_blocks=533)
+    inv = lib.msa_workspace_bytes(0, 8192, 1, ctypes.byref(d))
+    # bitmap over (group, block) keys x ceil(rows/32) words + per-key counts, 256-byte aligned
+    assert inv == ((8 * 533 * 256 * 4 + 255) // 256) * 256 + ((8 * 533 * 4 + 255) // 256) * 256
+    dec = lib.msa_workspace_bytes(1, 8, 0, ctypes.byref(good_dims()))
+    assert dec == ((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
+    assert lib.msa_workspace_bytes(9, 8, 1, ctypes.byref(d)) == 0
+    # too small a workspace is refused before any launch
+    rc = lib.msa_invert_selection(FAKE, FAKE, 8192, 1, ctypes.byref(d), FAKE, FAKE, FAKE, ctypes.c_size_t(inv - 1),
+                                  FAKE, None)
+    assert rc == 6
+    rc = lib.msa_sparse_attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 4096, ctypes.byref(good_dims()), FAKE, FAKE,
+                                    FAKE, ctypes.c_size_t(dec - 1), FAKE, None)
+    assert rc == 6
+
+
+def test_package_import_fails_loudly_without_library(tmp_path):
+    """The binding has no fallback: with the shared library missing, import raises."""
+    import subprocess
+    import sys
+    import shutil
+    pkg = os.path.join(ROOT, "block_sparse_attention_06_gb300")
+    dst = tmp_path / "block_sparse_attention_06_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("libmsa.so", "_build", "__pycache__"))
+    code = "import block_sparse_attention_06_gb300"
+    res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
+    assert res.returncode != 0 and "libmsa.so is not built" in res.stderr

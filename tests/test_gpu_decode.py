@@ -1,0 +1,115 @@
+"""Decode path on the GPU against the fp64 oracle: index scoring, top-k, page
+tables, paged sparse attention -- through the C ABI, on seeded workloads."""
+import pytest
+import torch
+
+import msa_inputs as mi
+import oracle
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import block_sparse_attention_06_gb300 as m
+    return m
+
+
+def _run_decode(m, case):
+    dims = m.dims_of(case)
+    step = m.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.seq_lens,
+         case.q_pos)
+    m.msa_check(step.err)
+    torch.cuda.synchronize()
+    return step
+
+
+def _check_decode(m, case, rows=None):
+    step = _run_decode(m, case)
+    rows = list(range(case.n_rows)) if rows is None else rows
+    ref = P.oracle_decode_rows(case, rows)
+    idx = torch.as_tensor(rows)
+    q_pos = case.q_pos.cpu()[idx]
+    P.assert_scores(step.scores.cpu()[idx], ref["scores"], q_pos)
+    # top-k kernel on the oracle's scores (rounded to fp32) is bit-exact
+    sc32 = ref["scores"].float()
+    sel_on_ref = m.msa_topk_blocks(sc32.to(DEV), q_pos.to(DEV), m.dims_of(case))
+    ref_sel32 = oracle.topk(sc32.double(), q_pos, case.dims.topk)
+    assert torch.equal(sel_on_ref.cpu(), ref_sel32)
+    # end to end: selection agrees where unambiguous
+    gap = P.selection_gap(ref["scores"], q_pos, case.dims.topk)
+    gsel = step.sel.cpu()[idx]
+    P.assert_selection_where_unambiguous(gsel, ref["sel"], gap)
+    # page table + row lengths bit-exact for the GPU's own selection
+    pt, rl = oracle.page_table(gsel, case.block_table.cpu()[case.q_req.cpu()[idx].long()], q_pos + 1)
+    G = case.dims.G
+    grow = torch.cat([torch.arange(r * G, (r + 1) * G) for r in rows])
+    assert torch.equal(step.page_table.cpu()[grow], pt)
+    assert torch.equal(step.row_len.cpu()[grow], rl)
+    # attention against the oracle on the GPU's selection
+    o_ref, l_ref = P.oracle_attention_on(case, rows, gsel)
+    P.assert_out(step.out.cpu()[idx], o_ref)
+    P.assert_lse(step.lse.cpu()[idx], l_ref)
+    return step, ref
+
+
+def test_tiny_decode_steps(msa):
+    """16 decode steps after a 2048-token prefix (Hq=8, G=2, D=64, Di=32, k=4)."""
+    _, dec = mi.tiny_case(seed=1000, device=DEV)
+    _check_decode(msa, dec)
+
+
+@pytest.mark.parametrize("lens", [[1, 127, 128, 129, 300, 2049], [5000, 17, 128 * 16 + 5]])
+def test_ragged_small_decode(msa, lens):
+    case = mi.decode_case(lens, Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=200, needles_per_group=4,
+                          seed=77, device=DEV)
+    _check_decode(msa, case)
+
+
+@pytest.mark.parametrize("hq,g,d,di", [(16, 4, 64, 32), (16, 2, 128, 64), (32, 8, 64, 64)])
+def test_decode_shape_variants(msa, hq, g, d, di):
+    case = mi.decode_case([700, 1500, 3000], Hq=hq, G=g, D=d, Di=di, topk=5, pool_pages=60, needles_per_group=2,
+                          seed=5, device=DEV)
+    _check_decode(msa, case)
+
+
+def test_decode60k_full(msa):
+    case = mi.named_case("decode60k", device=DEV)
+    _check_decode(msa, case)
+
+
+@pytest.mark.parametrize("name,rows", [("ragged1", [0]), ("ragged8", None), ("ragged32", [0, 7, 19, 31]),
+                                       ("ragged64", [1, 10, 33, 63])])
+def test_ragged_sweep(msa, name, rows):
+    case = mi.named_case(name, device=DEV)
+    _check_decode(msa, case, rows)
+
+
+def test_decode1m(msa):
+    case = mi.named_case("decode1m", device=DEV)
+    step, ref = _check_decode(msa, case)
+    # the planted needles are found: every needle block is selected for its (request, group)
+    sel = step.sel.cpu()
+    hit = sum(int(j in sel[b, g].tolist()) for (b, g, j) in case.needles)
+    assert hit >= int(0.9 * len(case.needles))
+
+
+def test_out_of_range_page_is_flagged(msa):
+    case = mi.decode_case([600, 900], Hq=16, G=2, D=128, Di=64, topk=4, pool_pages=20, needles_per_group=1,
+                          seed=3, device=DEV)
+    bad_bt = case.block_table.clone()
+    bad_bt[1, 2] = case.n_pages + 5
+    dims = msa.dims_of(case)
+    step = msa.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, bad_bt, case.seq_lens, case.q_pos)
+    with pytest.raises(msa.MsaError) as ei:
+        msa.msa_check(step.err)
+    assert ei.value.status == 4
+    # the error word was cleared: a clean call passes
+    step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.seq_lens,
+         case.q_pos)
+    msa.msa_check(step.err)

@@ -1,0 +1,145 @@
+"""Prefill path on the GPU against the fp64 oracle: tensor-core index scoring,
+top-k, {q,blk}->{blk,q} inversion, KV-block-major attention partials and the
+Log-Sum-Exp merge -- through the C ABI, on seeded workloads."""
+import pytest
+import torch
+
+import msa_inputs as mi
+import oracle
+from tests import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import block_sparse_attention_06_gb300 as m
+    return m
+
+
+def _run(m, case):
+    dims = m.dims_of(case)
+    step = m.PrefillStep(dims, case.n_rows, case.n_req, DEV)
+    step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.q_req, case.q_pos)
+    m.msa_check(step.err)
+    torch.cuda.synchronize()
+    return step
+
+
+def _check_prefill(m, case, rows=None, check_partials=True):
+    step = _run(m, case)
+    n = case.n_rows
+    rows = list(range(n)) if rows is None else rows
+    idx = torch.as_tensor(rows)
+    q_pos, q_req = case.q_pos.cpu()[idx], case.q_req.cpu()[idx]
+    bt = case.block_table.cpu()
+    local_bt = bt[q_req.long()]
+    local = torch.arange(len(rows), dtype=torch.int32)
+    ref_sc = oracle.block_scores(case.q_idx.cpu()[idx], case.kidx_cache.cpu(), local_bt, local, q_pos, case.max_blocks)
+    P.assert_scores(step.scores.cpu()[idx], ref_sc, q_pos)
+    ref_sel = oracle.topk(ref_sc, q_pos, case.dims.topk)
+    gap = P.selection_gap(ref_sc, q_pos, case.dims.topk)
+    gsel = step.sel.cpu()[idx]
+    P.assert_selection_where_unambiguous(gsel, ref_sel, gap)
+    # inversion of the GPU's full selection is bit-exact
+    off, ent = oracle.invert(step.sel.cpu(), case.q_req.cpu(), case.n_req, case.max_blocks)
+    assert torch.equal(step.blk_off.cpu(), off)
+    assert torch.equal(step.blk_ent.cpu()[:int(off[-1])], ent)
+    # per-block partials (valid slots) and the merged output on the GPU's selection
+    if check_partials:
+        kc, vc = case.k_cache.cpu(), case.v_cache.cpu()
+        op, lp = oracle.block_partials(case.q.cpu()[idx], kc, vc, local_bt, local, q_pos, gsel, case.dims.sm_scale)
+        hpg = case.dims.Hq // case.dims.G
+        valid = (gsel >= 0).repeat_interleave(hpg, dim=1).transpose(1, 2)   # [rows][topk][Hq]
+        P.assert_lse(step.lse_part.cpu()[idx][valid], lp[valid], "lse_part")
+        P.assert_out(step.o_part.cpu()[idx][valid], op[valid], "o_part")
+    o_ref, l_ref = P.oracle_attention_on(case, rows, gsel)
+    P.assert_out(step.out.cpu()[idx], o_ref)
+    P.assert_lse(step.lse.cpu()[idx], l_ref)
+    return step
+
+
+def test_tiny_prefill(msa):
+    """2048 causal rows, Hq=8, G=2, D=64, Di=32, k=4 (16 blocks, 16 row tiles)."""
+    pre, _ = mi.tiny_case(seed=1000, device=DEV)
+    _check_prefill(msa, pre)
+
+
+@pytest.mark.parametrize("prefix,chunk", [(1000, 300), (0, 257), (127, 1)])
+def test_small_prefill_ragged(msa, prefix, chunk):
+    case = mi.prefill_case(prefix, chunk, Hq=16, G=2, D=128, Di=64, topk=6, pool_pages=40, seed=12, device=DEV)
+    _check_prefill(msa, case)
+
+
+@pytest.mark.parametrize("hq,g,d,di", [(32, 8, 128, 64), (16, 4, 64, 32), (8, 2, 128, 32)])
+def test_prefill_shape_variants(msa, hq, g, d, di):
+    case = mi.prefill_case(2100, 400, Hq=hq, G=g, D=d, Di=di, topk=8, pool_pages=40, seed=13, device=DEV)
+    _check_prefill(msa, case)
+
+
+def test_prefill68k_sampled(msa):
+    """8192-row chunk on a 60,000-token prefix, full launch; oracle on sampled rows
+    (first/last tile, a span boundary, the ragged positions around block edges)."""
+    case = mi.named_case("prefill68k", device=DEV)
+    rows = [0, 1, 127, 128, 255, 256, 1000, 4095, 4096, 6000, 8190, 8191]
+    _check_prefill(msa, case, rows, check_partials=True)
+
+
+def test_topk_bit_exact_on_oracle_scores(msa):
+    """The top-k kernel on the oracle's scores, with ties and signed zeros planted."""
+    gen = torch.Generator().manual_seed(4)
+    n_rows, G, mb, k = 300, 8, 600, 16
+    vals = torch.tensor([-3.0, -0.0, 0.0, 0.5, 1.25, 1.25, 7.0], dtype=torch.float64)
+    scores = vals[torch.randint(0, len(vals), (n_rows, G, mb), generator=gen)]
+    scores += torch.randn(n_rows, G, mb, generator=gen, dtype=torch.float64).round() * 0.5
+    q_pos = torch.randint(0, mb * 128, (n_rows,), generator=gen, dtype=torch.int32)
+    q_pos[:5] = torch.tensor([0, 127, 128, 16 * 128, 599 * 128 + 5], dtype=torch.int32)
+    sc32 = scores.float()
+    dims = msa.Dims(64, G, 128, 64, k, mb)
+    got = msa.msa_topk_blocks(sc32.to(DEV), q_pos.to(DEV), dims)
+    want = oracle.topk(sc32.double(), q_pos, k)
+    assert torch.equal(got.cpu(), want)
+
+
+@pytest.mark.parametrize("mb", [1500, 8192, 16384])
+def test_topk_long_candidate_lists(msa, mb):
+    gen = torch.Generator().manual_seed(mb)
+    n_rows, G, k = 4, 8, 16
+    scores = torch.randn(n_rows, G, mb, generator=gen).round(decimals=1)   # many ties
+    q_pos = torch.tensor([mb * 128 - 1, 5000, 129, (mb // 2) * 128 + 7], dtype=torch.int32)
+    dims = msa.Dims(64, G, 128, 64, k, mb)
+    got = msa.msa_topk_blocks(scores.to(DEV), q_pos.to(DEV), dims)
+    assert torch.equal(got.cpu(), oracle.topk(scores.double(), q_pos, k))
+
+
+def test_invert_bit_exact_multi_request(msa):
+    gen = torch.Generator().manual_seed(8)
+    n_rows, G, k, n_req, mb = 1000, 4, 7, 3, 50
+    q_req = torch.randint(0, n_req, (n_rows,), generator=gen, dtype=torch.int32)
+    sel = torch.full((n_rows, G, k), -1, dtype=torch.int32)
+    for q in range(n_rows):
+        for g in range(G):
+            c = int(torch.randint(1, k + 1, (1,), generator=gen))
+            sel[q, g, :c] = torch.randperm(mb, generator=gen)[:c].sort().values.to(torch.int32)
+    dims = msa.Dims(16, G, 128, 64, k, mb)
+    off, ent = msa.msa_invert_selection(sel.to(DEV), q_req.to(DEV), n_req, dims)
+    roff, rent = oracle.invert(sel, q_req, n_req, mb)
+    assert torch.equal(off.cpu(), roff)
+    assert torch.equal(ent.cpu()[:int(roff[-1])], rent)
+
+
+def test_lse_merge_matches_oracle(msa):
+    gen = torch.Generator().manual_seed(2)
+    n_rows, G, Hq, D, k = 64, 4, 32, 128, 9
+    sel = torch.randint(-1, 20, (n_rows, G, k), generator=gen, dtype=torch.int32)
+    o = torch.randn(n_rows, k, Hq, D, generator=gen).to(torch.bfloat16)
+    lse = torch.randn(n_rows, k, Hq, generator=gen) * 3
+    dims = msa.Dims(Hq, G, D, 64, k, 20)
+    out, l = msa.msa_lse_merge(o.to(DEV), lse.to(DEV), sel.to(DEV), dims)
+    valid = (sel >= 0).repeat_interleave(Hq // G, dim=1).transpose(1, 2)
+    lse_m = torch.where(valid, lse.double(), torch.tensor(float("-inf"), dtype=torch.float64))
+    ro, rl = oracle.lse_merge(o.double() * valid[..., None], lse_m)
+    P.assert_out(out.cpu(), ro)
+    P.assert_lse(l.cpu(), rl)
