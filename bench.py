@@ -42,7 +42,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-benchmark")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="time one workload alone (profiling); the JSON line then omits the other")
+    ap.add_argument("--prefill-prefix", type=int, default=60000, help="cached tokens before the prefill chunk")
+    ap.add_argument("--prefill-chunk", type=int, default=8192, help="new query rows in the prefill chunk")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     return ap.parse_args()
 
 
@@ -177,7 +181,34 @@ def run_msa(args, rank, world, local):
     peaks, peak_src = load_peaks()
     K, W = args.steps, args.warmup
 
-    # ---------------- decode headline
+    line = {}
+    clocks = ClockSampler(local).start()
+    case = None
+    if args.only in ("all", "decode"):
+        dec, case = bench_decode(args, rank, world, local, dev, peaks, peak_src)
+        line.update(dec)
+    if args.only in ("all", "prefill"):
+        line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src)
+    line["clocks"] = clocks.stop()
+    if case is not None:
+        line["cpu_baseline"] = (cpu_baseline_decode(rank, case=case)
+                                if rank == 0 and not args.no_cpu_baseline else None)
+    if args.only == "prefill":
+        pre = line["prefill"]
+        line = {"metric": METRIC, "value": pre["value"], "unit": pre["unit"], "n_gpus": world, "steps": K,
+                "warmup": W, "ms_per_step": pre["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+                "config": pre["config"], "gpu_launches": pre["gpu_launches"], "roofline": pre["roofline"],
+                "clocks": line["clocks"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(args, rank, world, local, dev, peaks, peak_src):
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+    K, W = args.steps, args.warmup
     case = mi.named_case("decode60k", device=dev)
     dims = msa.dims_of(case)
     B = case.n_rows
@@ -191,7 +222,6 @@ def run_msa(args, rank, world, local):
     s1_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     s1_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local).start()
     barrier(world)
     torch.cuda.synchronize()
     t0.record()
@@ -241,59 +271,7 @@ def run_msa(args, rank, world, local):
     msa.msa_check(step.err)
     e2e_value = aggregate_throughput(B * K, world, e2e_ms / 1e3)
 
-    # ---------------- prefill chunk
-    prefill = None
-    if not args.no_prefill:
-        del step, case
-        torch.cuda.empty_cache()
-        pc = mi.named_case("prefill68k", device=dev)
-        pd = msa.dims_of(pc)
-        ps = msa.PrefillStep(pd, pc.n_rows, pc.n_req, dev)
-        pcall = lambda: ps(pc.q, pc.q_idx, pc.k_cache, pc.v_cache, pc.kidx_cache, pc.block_table, pc.q_req,
-                           pc.q_pos)
-        for _ in range(W):
-            pcall()
-        msa.msa_check(ps.err)
-        torch.cuda.synchronize()
-        a_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        a_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize()
-        p0.record()
-        for k in range(K):
-            ps.select(pc.q_idx, pc.kidx_cache, pc.block_table, pc.q_req, pc.q_pos)
-            a_b[k].record()
-            msa.msa_sparse_attn_prefill(pc.q, pc.k_cache, pc.v_cache, pc.block_table, pc.q_req, pc.q_pos,
-                                        ps.blk_off, ps.blk_ent, pd, ps.o_part, ps.lse_part, err_word=ps.err)
-            a_e[k].record()
-            msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, pd, ps.out, ps.lse, err_word=ps.err)
-        p1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        pre_ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
-        attn_ms = statistics.mean(a_b[k].elapsed_time(a_e[k]) for k in range(K))
-        msa.msa_check(ps.err)
-        flops = prefill_attention_flops(ps, pc)
-        tflops = flops / (attn_ms / 1e3) / 1e12
-        prefill = {
-            "metric": "MSA prefill q-tok/s", "value": aggregate_throughput(pc.n_rows * K, world, pre_ms / 1e3),
-            "unit": "q-tok/s", "ms_per_step": pre_ms / K, "steps": K,
-            "config": {"workload": "prefill68k", "prefix": 60000, "chunk": pc.n_rows, "Hq": pd.Hq, "G": pd.G,
-                       "D": pd.D, "Di": pd.Di, "topk": pd.topk},
-            "gpu_launches": ps.kernel_launches * K,
-            "roofline": {"bound": "tensor", "kernel": "k_attn_prefill", "achieved": tflops,
-                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tflops / peaks["bf16_tflops"], "traffic": NCU_TRAFFIC["k_attn_prefill"],
-                         "flops_per_launch": flops, "ms_per_launch": attn_ms,
-                         "peak_source": f"{peak_src} bf16_tflops (burst)"},
-        }
-    clk = clocks.stop()
-
-    # ---------------- CPU baseline: the oracle on host cores, bounded sample
-    cpu = cpu_baseline_decode(rank) if rank == 0 else None
-
-    line = {
+    return {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": dec_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, planted needle blocks)",
@@ -307,12 +285,63 @@ def run_msa(args, rank, world, local):
                      "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / K},
-        "clocks": clk,
-        "prefill": prefill,
-        "cpu_baseline": cpu,
+    }, case
+
+
+def bench_prefill(args, world, dev, peaks, peak_src):
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+    K, W = args.steps, args.warmup
+    if (args.prefill_prefix, args.prefill_chunk) == (60000, 8192):
+        pc = mi.named_case("prefill68k", device=dev)
+    else:
+        pc = mi.prefill_case(args.prefill_prefix, args.prefill_chunk, Hq=64, G=8, D=128, Di=64, topk=16,
+                             pool_pages=(args.prefill_prefix + args.prefill_chunk) // 128 + 64, seed=1002,
+                             device=dev)
+    pd = msa.dims_of(pc)
+    ps = msa.PrefillStep(pd, pc.n_rows, pc.n_req, dev)
+    pcall = lambda: ps(pc.q, pc.q_idx, pc.k_cache, pc.v_cache, pc.kidx_cache, pc.block_table, pc.q_req,
+                       pc.q_pos)
+    for _ in range(W):
+        pcall()
+    msa.msa_check(ps.err)
+    torch.cuda.synchronize()
+    a_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    a_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    p0.record()
+    for k in range(K):
+        ps.select(pc.q_idx, pc.kidx_cache, pc.block_table, pc.q_req, pc.q_pos)
+        a_b[k].record()
+        msa.msa_sparse_attn_prefill(pc.q, pc.k_cache, pc.v_cache, pc.block_table, pc.q_req, pc.q_pos,
+                                    ps.blk_off, ps.blk_ent, pd, ps.o_part, ps.lse_part, err_word=ps.err)
+        a_e[k].record()
+        msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, pd, ps.out, ps.lse, err_word=ps.err)
+    p1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    pre_ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
+    attn_ms = statistics.mean(a_b[k].elapsed_time(a_e[k]) for k in range(K))
+    msa.msa_check(ps.err)
+    flops = prefill_attention_flops(ps, pc)
+    tflops = flops / (attn_ms / 1e3) / 1e12
+    prefill = {
+        "metric": "MSA prefill q-tok/s", "value": aggregate_throughput(pc.n_rows * K, world, pre_ms / 1e3),
+        "unit": "q-tok/s", "ms_per_step": pre_ms / K, "steps": K,
+        "config": {"workload": "prefill68k" if pc.name == "prefill68k" else "prefill",
+                   "prefix": args.prefill_prefix, "chunk": pc.n_rows, "Hq": pd.Hq, "G": pd.G,
+                   "D": pd.D, "Di": pd.Di, "topk": pd.topk},
+        "gpu_launches": ps.kernel_launches * K,
+        "roofline": {"bound": "tensor", "kernel": "k_attn_prefill", "achieved": tflops,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16_tflops"], "traffic": NCU_TRAFFIC["k_attn_prefill"],
+                     "flops_per_launch": flops, "ms_per_launch": attn_ms,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return prefill
 
 
 def step_launches_decode() -> int:
