@@ -117,6 +117,8 @@ bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *di
     return true;
 }
 
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;

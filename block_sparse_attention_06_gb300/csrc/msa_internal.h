@@ -60,4 +60,7 @@ bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *di
 
 int sm_count();
 
+// Record the detail string that msa_last_error() returns on this thread.
+void set_last_error(const char *msg);
+
 }  // namespace msa

@@ -224,6 +224,33 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
                                     msa_stream_t stream);
 
 /*
+ * msa_sparse_attn_decode_noalloc -- the same computation as msa_sparse_attn_decode
+ * for callers that cannot allocate device memory.  The pages have no counterpart
+ * to it; it exists for callers like a serving engine that has reserved almost all
+ * HBM for its paged KV pool and routes every allocation through its own
+ * allocator, or a plugin host that forbids libraries from calling cudaMalloc.
+ * Such a caller cannot provide a workspace either, so the split-by-page partials
+ * go to a fixed 16 MiB device array inside the library instead.
+ *
+ *   Arguments, layouts and outputs: as msa_sparse_attn_decode, minus the workspace.
+ *   Limit: msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims) must not exceed 16 MiB
+ *   (for example B * G * topk <= 4064 rows x slots at Hq/G = 8, D = 128); larger
+ *   calls return MSA_ERR_WORKSPACE and enqueue nothing.
+ *   Allocation: none -- no cudaMalloc, cudaFree or allocating library routine.
+ *   The array is static device memory that every GPU loading the library holds
+ *   until the process exits.  The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress, with that device current); make that
+ *   first call before any stream capture.
+ *   Sharing: all calls use the same array and find in it what the previous call
+ *   left.  Calls whose kernels overlap on the GPU race on it, so the caller must
+ *   serialise them (one stream, or events between streams).
+ */
+msa_status_t msa_sparse_attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *page_table, const int32_t *row_len, int32_t B,
+                                            int32_t n_pages, const msa_dims_t *dims, void *out, float *lse,
+                                            int32_t *err_word, msa_stream_t stream);
+
+/*
  * msa_workspace_bytes -- device scratch needed by an operation:
  *   MSA_OP_INVERT: n_rows query rows, n_req requests;
  *   MSA_OP_DECODE: n_rows = B decode requests (n_req ignored).
