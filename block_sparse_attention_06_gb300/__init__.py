@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
         "msa_sparse_attn_prefill": [P, P, P, P, P, P, P, P, I, I, I, D, P, P, P, P],
         "msa_lse_merge": [P, P, P, I, D, P, P, P, P],
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
+        "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
         "msa_check": [P, P],
     }
     for name, argt in sigs.items():
@@ -301,6 +302,47 @@ def msa_sparse_attn_decode(q, k_cache, v_cache, page_table, row_len, dims: Dims,
     return out, lse
 
 
+def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, dims: Dims, scores=None,
+                    sel=None, page_table=None, row_len=None, out=None, lse=None, workspace=None, err_word=None):
+    """One whole decode step (index scan, top-k, page tables, sparse attention) in one
+    call; returns (out, lse, sel, page_table, row_len, scores)."""
+    B = q.shape[0]
+    _req(q, torch.bfloat16, "q", (B, dims.Hq, dims.D))
+    _req(q_idx, torch.bfloat16, "q_idx", (B, dims.G, dims.Di))
+    _req(k_cache, torch.bfloat16, "k_cache")
+    _req(v_cache, torch.bfloat16, "v_cache", tuple(k_cache.shape))
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (dims.page_size, dims.G, dims.D):
+        raise ValueError("k_cache must be [n_pages][128][G][D]")
+    _req(kidx_cache, torch.bfloat16, "kidx_cache", (k_cache.shape[0], dims.page_size, dims.G, dims.Di))
+    _req(block_table, torch.int32, "block_table", (B, dims.max_blocks))
+    _req(seq_lens, torch.int32, "seq_lens", (B,))
+    dev = q.device
+    f = dict(device=dev)
+    scores = torch.empty((B, dims.G, dims.max_blocks), dtype=torch.float32, **f) if scores is None else scores
+    sel = torch.empty((B, dims.G, dims.topk), dtype=torch.int32, **f) if sel is None else sel
+    if page_table is None:
+        page_table = torch.empty((B * dims.G, dims.topk), dtype=torch.int32, **f)
+    row_len = torch.empty((B * dims.G,), dtype=torch.int32, **f) if row_len is None else row_len
+    out = torch.empty((B, dims.Hq, dims.D), dtype=torch.bfloat16, **f) if out is None else out
+    lse = torch.empty((B, dims.Hq), dtype=torch.float32, **f) if lse is None else lse
+    _req(scores, torch.float32, "scores", (B, dims.G, dims.max_blocks))
+    _req(sel, torch.int32, "sel", (B, dims.G, dims.topk))
+    _req(page_table, torch.int32, "page_table", (B * dims.G, dims.topk))
+    _req(row_len, torch.int32, "row_len", (B * dims.G,))
+    _req(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
+    _req(lse, torch.float32, "lse", (B, dims.Hq))
+    need = msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, **f)
+    _req(workspace, torch.uint8, "workspace")
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_decode_step", _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(kidx_cache), _ptr(block_table),
+          _ptr(seq_lens), B, k_cache.shape[0], ctypes.byref(d), _ptr(scores), _ptr(sel), _ptr(page_table),
+          _ptr(row_len), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
+    return out, lse, sel, page_table, row_len, scores
+
+
 # ------------------------------------------------------------------ whole-path helpers
 
 def dims_of(case) -> Dims:
@@ -312,7 +354,10 @@ def dims_of(case) -> Dims:
 class DecodeStep:
     """One MSA decode step with preallocated buffers: index scoring -> top-k ->
     page table -> paged sparse attention.  Buffers are reused across calls so the
-    step can be replayed (and captured in a CUDA graph)."""
+    step can be replayed (and captured in a CUDA graph).
+
+    Calling the object runs the fused entry point msa_decode_step (three kernels);
+    composed() runs the same step through the four separate entry points."""
 
     def __init__(self, dims: Dims, B: int, n_req: int, n_pages: int, device):
         self.dims, self.B, self.n_req, self.n_pages = dims, B, n_req, n_pages
@@ -327,7 +372,7 @@ class DecodeStep:
                                      dtype=torch.uint8, **f)
         self.err = new_err_word(device)
         self.q_req = torch.arange(B, dtype=torch.int32, **f)
-        self.kernel_launches = 5   # score, top-k, page table, attention partials, merge
+        self.kernel_launches = 3   # index scan, selection (top-k + page table), attention with merge
 
     def scores_only(self, q_idx, kidx_cache, block_table, q_pos):
         return msa_index_score(q_idx, kidx_cache, block_table, self.q_req, q_pos, self.dims, MSA_PHASE_DECODE,
@@ -340,9 +385,14 @@ class DecodeStep:
         return msa_sparse_attn_decode(q, k_cache, v_cache, self.page_table, self.row_len, self.dims, self.out,
                                       self.lse, self.workspace, err_word=self.err)
 
-    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos):
+    def composed(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos):
         self.scores_only(q_idx, kidx_cache, block_table, q_pos)
         return self.rest(q, k_cache, v_cache, block_table, q_pos, seq_lens)
+
+    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos=None):
+        msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, self.dims, self.scores,
+                        self.sel, self.page_table, self.row_len, self.out, self.lse, self.workspace, self.err)
+        return self.out, self.lse
 
 
 class PrefillStep:

@@ -11,9 +11,10 @@
 //     m16n8k16 bf16 MMA (tokens = M), the way the page's own index-scoring kernel
 //     uses 128-token tiles as M; decode attention moves ~8 flop per byte, so
 //     these small legacy tiles keep it HBM-bound;
-//   - each work item writes a normalised partial (O, lse) to the workspace and a
-//     second kernel merges the partials of a row by Log-Sum-Exp (the reduction of
-//     section KV 块主序稀疏注意力).
+//   - each work item writes a normalised partial (O, lse) to the workspace and
+//     counts itself done on the row's counter; the work item that finishes a row
+//     last merges the row's partials by Log-Sum-Exp (the reduction of section
+//     KV 块主序稀疏注意力) and writes the output, so no second kernel runs.
 #include "msa_device.cuh"
 #include "msa_internal.h"
 
@@ -61,36 +62,23 @@ struct DecodeSmem {
     float m[8];
     float l[8];    // sum of the bf16-rounded probabilities
     float le[8];   // exact fp32 sum
+    float mlse[32 * 8];   // merge: lse of every (slot, head) of the row
     uint64_t kbar, vbar;
     int abort;
+    int last;
 };
 
+// One (row, page) work item: S^T = K Q^T on the tensor cores (tokens = M, the
+// group's heads = N), softmax over the page's n_tok tokens, O^T = V^T P^T, and the
+// normalised partial (O, lse) of the page into o_out / lse_out.
 template <int D, int HPG>
-__global__ void __launch_bounds__(128) k_attn_decode_part(
-    const uint16_t *__restrict__ q, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const int32_t *__restrict__ pt,
-    const int32_t *__restrict__ row_len, int G, int topk, int n_pages, float sm_scale,
-    float *__restrict__ o_ws, float *__restrict__ lse_ws, int32_t *err) {
-    static_assert(HPG == 4 || HPG == 8, "heads per group");
+__device__ __forceinline__ void attend_page(DecodeSmem<D, HPG> &sm, const uint16_t *__restrict__ q,
+                                            const CUtensorMap &kmap, const CUtensorMap &vmap, int r, int G,
+                                            int page, int n_tok, float sm_scale, float *__restrict__ o_out,
+                                            float *__restrict__ lse_out, int32_t *err) {
     constexpr int NB = D / 64;   // TMA boxes per tile
-    extern __shared__ uint8_t smem_raw[];
-    DecodeSmem<D, HPG> &sm =
-        *reinterpret_cast<DecodeSmem<D, HPG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-
-    const int slot = blockIdx.x, r = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = r / G, g = r - b * G;
-    float *lse_out = lse_ws + (size_t(r) * topk + slot) * HPG;
-    float *o_out = o_ws + (size_t(r) * topk + slot) * HPG * D;
-
-    const int page = pt[size_t(r) * topk + slot];
-    const int n_tok = min(128, row_len[r] - slot * 128);
-    if (page < 0 || n_tok <= 0 || page >= n_pages) {
-        if (page >= n_pages && tid == 0) raise_flag(err, MSA_FLAG_BOUNDS);
-        if (tid < HPG) lse_out[tid] = -INFINITY;
-        return;
-    }
-
     if (tid == 0) {
         mbar_init(&sm.kbar, 1);
         mbar_init(&sm.vbar, 1);
@@ -249,49 +237,105 @@ __global__ void __launch_bounds__(128) k_attn_decode_part(
     if (tid < HPG) lse_out[tid] = (k_ok && v_ok) ? (sm.m[tid] + log2f(sm.le[tid])) * kLn2 : -INFINITY;
 }
 
-// Merge the partials of one row r = b*G + g: out[b][g*HPG + n][:] and lse.
+// Merge the topk partials of row r = b*G + g into out[b][g*HPG + n][:] and lse.
+// Called by all 128 threads of the CTA that finished the row last; the partials
+// of the other CTAs are read through L2 (ld.global.cg), never a stale L1 line.
 template <int D, int HPG>
-__global__ void __launch_bounds__(HPG * D / 4) k_attn_decode_merge(
-    const float *__restrict__ o_ws, const float *__restrict__ lse_ws, int G, int topk,
-    uint16_t *__restrict__ out, float *__restrict__ lse) {
-    const int r = blockIdx.x;
+__device__ __forceinline__ void merge_row(DecodeSmem<D, HPG> &sm, const float *__restrict__ o_ws,
+                                          const float *__restrict__ lse_ws, int r, int G, int topk,
+                                          uint16_t *__restrict__ out, float *__restrict__ lse) {
     const int tid = threadIdx.x;
-    const int n = tid / (D / 4);
-    const int d = (tid % (D / 4)) * 4;
-    const int b = r / G, g = r - b * G;
     const float *ls = lse_ws + size_t(r) * topk * HPG;
+    for (int i = tid; i < topk * HPG; i += 128) sm.mlse[i] = __ldcg(ls + i);
+    __syncthreads();
+    constexpr int TPH = D / 8;              // threads per head, 8 columns each
+    const int n = tid / TPH;
+    const int d = (tid % TPH) * 8;
+    if (n >= HPG) return;
+    const int b = r / G, g = r - b * G;
     float m = -INFINITY;
-    for (int s = 0; s < topk; ++s) m = fmaxf(m, ls[s * HPG + n]);
+    for (int s = 0; s < topk; ++s) m = fmaxf(m, sm.mlse[s * HPG + n]);
     const size_t h = size_t(b) * G * HPG + size_t(g) * HPG + n;
     uint16_t *o = out + h * D + d;
     if (m == -INFINITY) {
-        *reinterpret_cast<uint2 *>(o) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint4 *>(o) = make_uint4(0u, 0u, 0u, 0u);
         if (d == 0) lse[h] = -INFINITY;
         return;
     }
     float sum = 0.f;
     for (int s = 0; s < topk; ++s) {
-        const float l = ls[s * HPG + n];
+        const float l = sm.mlse[s * HPG + n];
         if (l != -INFINITY) sum += __expf(l - m);
     }
     const float tot = m + __logf(sum);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const float *src = o_ws + (size_t(r) * topk * HPG + n) * D + d;
+#pragma unroll 4
     for (int s = 0; s < topk; ++s) {
-        const float l = ls[s * HPG + n];
+        const float l = sm.mlse[s * HPG + n];
         if (l == -INFINITY) continue;
         const float w = __expf(l - tot);
-        const float4 v = *reinterpret_cast<const float4 *>(o_ws + ((size_t(r) * topk + s) * HPG + n) * D + d);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(src + size_t(s) * HPG * D));
+        const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(src + size_t(s) * HPG * D + 4));
+        acc[0] = fmaf(w, v0.x, acc[0]);
+        acc[1] = fmaf(w, v0.y, acc[1]);
+        acc[2] = fmaf(w, v0.z, acc[2]);
+        acc[3] = fmaf(w, v0.w, acc[3]);
+        acc[4] = fmaf(w, v1.x, acc[4]);
+        acc[5] = fmaf(w, v1.y, acc[5]);
+        acc[6] = fmaf(w, v1.z, acc[6]);
+        acc[7] = fmaf(w, v1.w, acc[7]);
     }
-    *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    *reinterpret_cast<uint4 *>(o) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     if (d == 0) lse[h] = tot;
 }
 
+template <int D, int HPG>
+__global__ void __launch_bounds__(128) k_attn_decode(
+    const uint16_t *__restrict__ q, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap vmap, const int32_t *__restrict__ pt,
+    const int32_t *__restrict__ row_len, int G, int topk, int n_pages, float sm_scale,
+    float *__restrict__ o_ws, float *__restrict__ lse_ws, int32_t *__restrict__ counters,
+    uint16_t *__restrict__ out, float *__restrict__ lse, int32_t *err) {
+    static_assert(HPG == 4 || HPG == 8, "heads per group");
+    extern __shared__ uint8_t smem_raw[];
+    DecodeSmem<D, HPG> &sm =
+        *reinterpret_cast<DecodeSmem<D, HPG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int slot = blockIdx.x, r = blockIdx.y;
+    const int tid = threadIdx.x;
+    float *lse_out = lse_ws + (size_t(r) * topk + slot) * HPG;
+    float *o_out = o_ws + (size_t(r) * topk + slot) * HPG * D;
+
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    pdl_wait();   // the page table comes from the previous kernel
+    pdl_trigger();
+
+    const int page = pt[size_t(r) * topk + slot];
+    const int n_tok = min(128, row_len[r] - slot * 128);
+    if (page < 0 || n_tok <= 0 || page >= n_pages) {
+        if (page >= n_pages && tid == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+        if (tid < HPG) lse_out[tid] = -INFINITY;
+    } else {
+        attend_page<D, HPG>(sm, q, kmap, vmap, r, G, page, n_tok, sm_scale, o_out, lse_out, err);
+    }
+
+    // Count this work item done; the last of the row's topk work items merges.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sm.last = atomicAdd(counters + r, 1) == topk - 1;
+    __syncthreads();
+    if (!sm.last) return;
+    __threadfence();
+    if (tid == 0) counters[r] = 0;   // leave the counter clean
+    merge_row<D, HPG>(sm, o_ws, lse_ws, r, G, topk, out, lse);
+}
+
+
 struct DecodeWs {
-    size_t o_off, lse_off, bytes;
+    size_t o_off, lse_off, cnt_off, bytes;
 };
 
 inline DecodeWs decode_ws(int B, const Shape &s) {
@@ -299,38 +343,45 @@ inline DecodeWs decode_ws(int B, const Shape &s) {
     const size_t units = size_t(B) * s.G * s.topk;
     w.o_off = 0;
     w.lse_off = (units * s.hpg * s.D * 4 + 255) & ~size_t(255);
-    w.bytes = w.lse_off + ((units * s.hpg * 4 + 255) & ~size_t(255));
+    w.cnt_off = w.lse_off + ((units * s.hpg * 4 + 255) & ~size_t(255));
+    w.bytes = w.cnt_off + ((size_t(B) * s.G * 4 + 255) & ~size_t(255));
     return w;
 }
 
 template <int D, int HPG>
 cudaError_t launch_t(const void *q, const CUtensorMap &km, const CUtensorMap &vm, const int32_t *pt,
                      const int32_t *row_len, int B, int n_pages, const Shape &s, void *out, float *lse,
-                     void *ws, int32_t *err, cudaStream_t st) {
+                     void *ws, int32_t *err, cudaStream_t st, bool counters_zeroed, bool pdl) {
     const DecodeWs w = decode_ws(B, s);
-    float *o_ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w.o_off);
-    float *l_ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + w.lse_off);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    float *o_ws = reinterpret_cast<float *>(base + w.o_off);
+    float *l_ws = reinterpret_cast<float *>(base + w.lse_off);
+    int32_t *cnt = reinterpret_cast<int32_t *>(base + w.cnt_off);
+    cudaError_t e;
+    if (!counters_zeroed) {
+        e = cudaMemsetAsync(cnt, 0, size_t(B) * s.G * 4, st);
+        if (e != cudaSuccess) return e;
+    }
     const size_t smem = sizeof(DecodeSmem<D, HPG>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_part<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
+    e = cudaFuncSetAttribute(k_attn_decode<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(unsigned(s.topk), unsigned(B * s.G));
-    k_attn_decode_part<D, HPG><<<grid, 128, smem, st>>>(static_cast<const uint16_t *>(q), km, vm, pt, row_len, s.G,
-                                                        s.topk, n_pages, s.sm_scale, o_ws, l_ws, err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    k_attn_decode_merge<D, HPG><<<unsigned(B * s.G), HPG * D / 4, 0, st>>>(o_ws, l_ws, s.G, s.topk,
-                                                                          static_cast<uint16_t *>(out), lse);
-    return cudaGetLastError();
+    return launch_kernel(k_attn_decode<D, HPG>, dim3(unsigned(s.topk), unsigned(B * s.G)), dim3(128), smem, st,
+                         pdl && counters_zeroed, static_cast<const uint16_t *>(q), km, vm, pt, row_len, s.G, s.topk,
+                         n_pages, s.sm_scale, o_ws, l_ws, cnt, static_cast<uint16_t *>(out), lse, err);
 }
 
 }  // namespace
 
 size_t decode_workspace_bytes(int B, const Shape &s) { return decode_ws(B, s).bytes; }
 
+int32_t *decode_ws_counters(void *ws, int B, const Shape &s) {
+    return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + decode_ws(B, s).cnt_off);
+}
+
 cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *pt,
                                const int32_t *row_len, int B, int n_pages, const Shape &s, void *out,
-                               float *lse, void *ws, int32_t *err, cudaStream_t st) {
+                               float *lse, void *ws, int32_t *err, cudaStream_t st, bool counters_zeroed,
+                               bool pdl) {
     if (B <= 0) return cudaSuccess;
     alignas(64) CUtensorMap km, vm;
     const uint64_t dims[4] = {uint64_t(s.D), uint64_t(s.G), 128ull, uint64_t(n_pages)};
@@ -339,10 +390,11 @@ cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v
     const char *why = nullptr;
     if (!encode_tensor_map(&km, 4, k_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
     if (!encode_tensor_map(&vm, 4, v_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
-    if (s.D == 128 && s.hpg == 8) return launch_t<128, 8>(q, km, vm, pt, row_len, B, n_pages, s, out, lse, ws, err, st);
-    if (s.D == 128 && s.hpg == 4) return launch_t<128, 4>(q, km, vm, pt, row_len, B, n_pages, s, out, lse, ws, err, st);
-    if (s.D == 64 && s.hpg == 8) return launch_t<64, 8>(q, km, vm, pt, row_len, B, n_pages, s, out, lse, ws, err, st);
-    if (s.D == 64 && s.hpg == 4) return launch_t<64, 4>(q, km, vm, pt, row_len, B, n_pages, s, out, lse, ws, err, st);
+#define MSA_AD_CASE(DD, HH)                                                                                    \
+    if (s.D == DD && s.hpg == HH)                                                                              \
+        return launch_t<DD, HH>(q, km, vm, pt, row_len, B, n_pages, s, out, lse, ws, err, st, counters_zeroed, pdl);
+    MSA_AD_CASE(128, 8) MSA_AD_CASE(128, 4) MSA_AD_CASE(64, 8) MSA_AD_CASE(64, 4)
+#undef MSA_AD_CASE
     return cudaErrorNotSupported;
 }
 

@@ -19,8 +19,8 @@ template <int G, int DI>
 __global__ void __launch_bounds__(256) k_score_decode(
     const uint16_t *__restrict__ q_idx, const uint8_t *__restrict__ kidx,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req,
-    const int32_t *__restrict__ q_pos, int n_req, int n_pages, int max_blocks,
-    float *__restrict__ scores, int32_t *err) {
+    const int32_t *__restrict__ q_pos, const int32_t *__restrict__ seq_lens, int n_req, int n_pages,
+    int max_blocks, float *__restrict__ scores, int32_t *err) {
     constexpr int SUBS = DI / 8;             // 16-byte chunks per (token, group)
     constexpr int CPT = G * SUBS;            // chunks per token
     constexpr int TPP = 256 / CPT;           // tokens per pass of the CTA
@@ -34,8 +34,11 @@ __global__ void __launch_bounds__(256) k_score_decode(
     const int tid = threadIdx.x;
     float *out = scores + size_t(r) * G * max_blocks + j;
 
-    const int p = q_pos[r];
-    const int req = q_req[r];
+    pdl_trigger();   // the selection kernel may start launching once every scan CTA runs
+
+    // rows are either (q_req, q_pos) pairs or the requests themselves at seq_lens - 1
+    const int p = q_pos ? q_pos[r] : seq_lens[r] - 1;
+    const int req = q_req ? q_req[r] : r;
     if (p < 0 || req < 0 || req >= n_req || (p >> 7) >= max_blocks) {
         if (tid < G) out[size_t(tid) * max_blocks] = -INFINITY;
         if (tid == 0 && j == 0) raise_flag(err, MSA_FLAG_BOUNDS);
@@ -97,32 +100,44 @@ __global__ void __launch_bounds__(256) k_score_decode(
 
 template <int G, int DI>
 cudaError_t launch_g(const void *q_idx, const void *kidx, const int32_t *bt, const int32_t *q_req,
-                     const int32_t *q_pos, int n_rows, int n_req, int n_pages, int max_blocks,
-                     float *scores, int32_t *err, cudaStream_t st) {
+                     const int32_t *q_pos, const int32_t *seq_lens, int n_rows, int n_req, int n_pages,
+                     int max_blocks, float *scores, int32_t *err, cudaStream_t st) {
     const long long grid = 1LL * n_rows * max_blocks;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     k_score_decode<G, DI><<<unsigned(grid), 256, 0, st>>>(
-        static_cast<const uint16_t *>(q_idx), static_cast<const uint8_t *>(kidx), bt, q_req, q_pos, n_req,
-        n_pages, max_blocks, scores, err);
+        static_cast<const uint16_t *>(q_idx), static_cast<const uint8_t *>(kidx), bt, q_req, q_pos, seq_lens,
+        n_req, n_pages, max_blocks, scores, err);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32_t *block_table,
-                                const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
-                                int n_pages, const Shape &s, float *scores, int32_t *err,
-                                cudaStream_t st) {
-#define MSA_SD_CASE(GG, DD)                                                                        \
-    if (s.G == GG && s.Di == DD)                                                                   \
-        return launch_g<GG, DD>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages,   \
+static cudaError_t launch_any(const void *q_idx, const void *kidx, const int32_t *block_table, const int32_t *q_req,
+                              const int32_t *q_pos, const int32_t *seq_lens, int n_rows, int n_req, int n_pages,
+                              const Shape &s, float *scores, int32_t *err, cudaStream_t st) {
+#define MSA_SD_CASE(GG, DD)                                                                               \
+    if (s.G == GG && s.Di == DD)                                                                          \
+        return launch_g<GG, DD>(q_idx, kidx, block_table, q_req, q_pos, seq_lens, n_rows, n_req, n_pages, \
                                 s.max_blocks, scores, err, st);
     MSA_SD_CASE(1, 32) MSA_SD_CASE(1, 64) MSA_SD_CASE(2, 32) MSA_SD_CASE(2, 64)
     MSA_SD_CASE(4, 32) MSA_SD_CASE(4, 64) MSA_SD_CASE(8, 32) MSA_SD_CASE(8, 64)
     MSA_SD_CASE(16, 32) MSA_SD_CASE(16, 64)
 #undef MSA_SD_CASE
     return cudaErrorNotSupported;
+}
+
+cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
+                                int n_pages, const Shape &s, float *scores, int32_t *err,
+                                cudaStream_t st) {
+    return launch_any(q_idx, kidx, block_table, q_req, q_pos, nullptr, n_rows, n_req, n_pages, s, scores, err, st);
+}
+
+cudaError_t launch_score_decode_seq(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                    const int32_t *seq_lens, int B, int n_pages, const Shape &s,
+                                    float *scores, int32_t *err, cudaStream_t st) {
+    return launch_any(q_idx, kidx, block_table, nullptr, nullptr, seq_lens, B, B, n_pages, s, scores, err, st);
 }
 
 }  // namespace msa

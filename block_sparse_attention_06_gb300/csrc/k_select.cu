@@ -27,6 +27,60 @@ __device__ __forceinline__ uint64_t block_key(float s, int j, int32_t *err) {
 
 __device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
+// The n best keys (n <= 32) among a warp's candidate keys, best first: lane i < n
+// receives the i-th best key, every other lane 0.  A key of 0 is "no candidate";
+// when fewer than n candidates exist the missing ranks are 0 too.  Each round
+// takes the largest key below the previous round's, so equal scores are ordered
+// by the block id inside the key and nothing is picked twice.
+template <int PER>
+__device__ __forceinline__ uint64_t warp_top_n(const uint64_t (&keys)[PER], int n) {
+    const int lane = threadIdx.x & 31;
+    uint64_t prev = ~0ull, mine = 0;
+    for (int round = 0; round < n; ++round) {
+        uint64_t best = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const uint64_t k = keys[i];
+            best = (k < prev && k > best) ? k : best;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
+        prev = best;
+        if (lane == round) mine = best;
+    }
+    return mine;
+}
+
+// Position of this lane's block id among the ids held by lanes 0 .. n-1
+// (ascending order); only meaningful for lanes < n.
+__device__ __forceinline__ int rank_ascending(int id, int n) {
+    int rank = 0;
+    for (int l = 0; l < n; ++l) {
+        const int other = __shfl_sync(0xffffffffu, id, l);
+        rank += other < id ? 1 : 0;
+    }
+    return rank;
+}
+
+// CTA-wide top-n: every warp reduces its own keys to its n best, then warp 0
+// takes the n best of those.  Returns, in warp 0, the lane's key as warp_top_n
+// does; other warps return 0.  `stage` holds NT keys of shared memory.
+template <int NT, int PER>
+__device__ __forceinline__ uint64_t cta_top_n(const uint64_t (&keys)[PER], int n, uint64_t *stage) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x;
+    stage[tid] = warp_top_n<PER>(keys, n);
+    __syncthreads();
+    uint64_t mine = 0;
+    if (tid < 32) {
+        uint64_t k2[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) k2[w] = stage[tid + 32 * w];
+        mine = warp_top_n<NW>(k2, n);
+    }
+    return mine;
+}
+
 // One warp per (row, group); keys of candidates j = lane + 32 * i live in registers.
 template <int PER>
 __global__ void __launch_bounds__(256) k_topk_warp(const float *__restrict__ scores,
@@ -53,41 +107,23 @@ __global__ void __launch_bounds__(256) k_topk_warp(const float *__restrict__ sco
         const int j = lane + 32 * i;
         keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
     }
-    int mine = 0x7fffffff;
-    uint64_t prev = ~0ull;
-    for (int round = 0; round < k_eff - 1; ++round) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const uint64_t k = keys[i];
-            best = (k < prev && k > best) ? k : best;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
-        prev = best;
-        if (lane == round) mine = int(~uint32_t(best));
-    }
-    int rank = 0;
-    for (int l = 0; l < k_eff - 1; ++l) {
-        const int other = __shfl_sync(0xffffffffu, mine, l);
-        rank += other < mine ? 1 : 0;
-    }
+    const int mine = int(~uint32_t(warp_top_n<PER>(keys, k_eff - 1)));
+    const int rank = rank_ascending(mine, k_eff - 1);
     if (lane < k_eff - 1) out[rank] = mine;
     if (lane == 0) out[k_eff - 1] = own;
     for (int i = k_eff + lane; i < topk; i += 32) out[i] = -1;
 }
 
-// One CTA of NT threads per (row, group) for long contexts.
+// One CTA of NT threads per (row, group) for long contexts: each warp keeps its
+// own best k-1, then warp 0 picks the best k-1 of those.
 template <int NT, int PER>
 __global__ void __launch_bounds__(NT) k_topk_cta(const float *__restrict__ scores,
                                                  const int32_t *__restrict__ q_pos, int G,
                                                  int max_blocks, int topk, int32_t *__restrict__ sel,
                                                  int32_t *err) {
-    constexpr int NW = NT / 32;
-    __shared__ uint64_t wbest[NW];
-    __shared__ int picked[32];
+    __shared__ uint64_t stage[NT];
     const int item = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int r = item / G;
     int32_t *out = sel + size_t(item) * topk;
     const int p = q_pos[r];
@@ -105,40 +141,143 @@ __global__ void __launch_bounds__(NT) k_topk_cta(const float *__restrict__ score
         const int j = tid + NT * i;
         keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
     }
-    uint64_t prev = ~0ull;
-    for (int round = 0; round < k_eff - 1; ++round) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const uint64_t k = keys[i];
-            best = (k < prev && k > best) ? k : best;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
-        if (lane == 0) wbest[warp] = best;
-        __syncthreads();
-        best = 0;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) best = max_u64(best, wbest[w]);
-        __syncthreads();
-        prev = best;
-        if (tid == 0) picked[round] = int(~uint32_t(best));
+    const uint64_t best = cta_top_n<NT, PER>(keys, k_eff - 1, stage);
+    if (tid < 32) {
+        const int mine = int(~uint32_t(best));
+        const int rank = rank_ascending(mine, k_eff - 1);
+        if (tid < k_eff - 1) out[rank] = mine;
+        if (tid == 0) out[k_eff - 1] = own;
+        for (int i = k_eff + tid; i < topk; i += 32) out[i] = -1;
     }
-    if (tid == 0) {
-        const int n = k_eff - 1;
-        for (int a = 1; a < n; ++a) {
-            const int v = picked[a];
-            int b = a - 1;
-            while (b >= 0 && picked[b] > v) {
-                picked[b + 1] = picked[b];
-                --b;
+}
+
+// ------------------------------------------------------------------ decode selection (fused)
+//
+// After the decode index scan, one launch turns a request's block scores into
+// its selection, its page tables and its row lengths ("Together AI 解析如何高效
+// 服务 MiniMax M3…", 将 MSA 与分页注意力集成: page tables per flattened (request,
+// group) row; 未来工作: the small top-k kernel fused with its neighbours).  Lane
+// i < k_eff of the row's warp owns slot i of the ascending selection.
+
+// Write the selection, page table and row length of row `item` (one warp).
+// `best` holds, in lanes 0 .. k_eff-2, the chosen non-own keys.
+__device__ __forceinline__ void emit_decode_row(uint64_t best, int item, int b, int L, int own, int k_eff,
+                                                int topk, int max_blocks, int n_pages,
+                                                const int32_t *__restrict__ block_table, int32_t *__restrict__ sel,
+                                                int32_t *__restrict__ pt, int32_t *__restrict__ row_len,
+                                                int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    int id = int(~uint32_t(best));
+    int slot = rank_ascending(id, k_eff - 1);
+    if (lane == k_eff - 1) {   // the own block is the largest id: last slot
+        id = own;
+        slot = k_eff - 1;
+    }
+    int tok = 0;
+    if (lane < k_eff) {
+        int page = -1;
+        if (id < 0 || id >= max_blocks) {
+            raise_flag(err, MSA_FLAG_BOUNDS);
+        } else {
+            page = block_table[size_t(b) * max_blocks + id];
+            if (page < 0 || page >= n_pages) {
+                raise_flag(err, MSA_FLAG_BOUNDS);
+                page = -1;
+            } else {
+                tok = max(0, min(128, L - id * 128));
             }
-            picked[b + 1] = v;
         }
-        for (int i = 0; i < n; ++i) out[i] = picked[i];
-        out[n] = own;
+        sel[size_t(item) * topk + slot] = id;
+        pt[size_t(item) * topk + slot] = page;
     }
-    for (int i = k_eff + tid; i < topk; i += NT) out[i] = -1;
+    for (int i = k_eff + lane; i < topk; i += 32) {
+        sel[size_t(item) * topk + i] = -1;
+        pt[size_t(item) * topk + i] = -1;
+    }
+    tok = warp_sum_i(tok);
+    if (lane == 0) row_len[item] = tok;
+}
+
+// One warp per (request, group) row, candidates in registers (PER per lane).
+template <int PER>
+__global__ void __launch_bounds__(256) k_decode_select_warp(
+    const float *__restrict__ scores, const int32_t *__restrict__ seq_lens,
+    const int32_t *__restrict__ block_table, int B, int G, int max_blocks, int topk, int n_pages,
+    int32_t *__restrict__ sel, int32_t *__restrict__ pt, int32_t *__restrict__ row_len,
+    int32_t *__restrict__ counters, int32_t *err) {
+    pdl_wait();   // the scores come from the scan kernel
+    pdl_trigger();
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (item >= B * G) return;
+    if (counters && lane == 0) counters[item] = 0;
+    const int b = item / G;
+    const int L = seq_lens[b];
+    const int p = L - 1;
+    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= 32 * PER) {
+        for (int i = lane; i < topk; i += 32) {
+            sel[size_t(item) * topk + i] = -1;
+            pt[size_t(item) * topk + i] = -1;
+        }
+        if (lane == 0) {
+            row_len[item] = 0;
+            raise_flag(err, MSA_FLAG_BOUNDS);
+        }
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const float *s = scores + size_t(item) * max_blocks;
+    uint64_t keys[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = lane + 32 * i;
+        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+    }
+    const uint64_t best = warp_top_n<PER>(keys, k_eff - 1);
+    emit_decode_row(best, item, b, L, own, k_eff, topk, max_blocks, n_pages, block_table, sel, pt, row_len, err);
+}
+
+// One CTA of NT threads per row for long contexts.
+template <int NT, int PER>
+__global__ void __launch_bounds__(NT) k_decode_select_cta(
+    const float *__restrict__ scores, const int32_t *__restrict__ seq_lens,
+    const int32_t *__restrict__ block_table, int B, int G, int max_blocks, int topk, int n_pages,
+    int32_t *__restrict__ sel, int32_t *__restrict__ pt, int32_t *__restrict__ row_len,
+    int32_t *__restrict__ counters, int32_t *err) {
+    __shared__ uint64_t stage[NT];
+    pdl_wait();
+    pdl_trigger();
+    const int item = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (counters && tid == 0) counters[item] = 0;
+    const int b = item / G;
+    const int L = seq_lens[b];
+    const int p = L - 1;
+    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= NT * PER) {
+        for (int i = tid; i < topk; i += NT) {
+            sel[size_t(item) * topk + i] = -1;
+            pt[size_t(item) * topk + i] = -1;
+        }
+        if (tid == 0) {
+            row_len[item] = 0;
+            raise_flag(err, MSA_FLAG_BOUNDS);
+        }
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const float *s = scores + size_t(item) * max_blocks;
+    uint64_t keys[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int j = tid + NT * i;
+        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+    }
+    const uint64_t best = cta_top_n<NT, PER>(keys, k_eff - 1, stage);
+    if (tid < 32)
+        emit_decode_row(best, item, b, L, own, k_eff, topk, max_blocks, n_pages, block_table, sel, pt, row_len,
+                        err);
 }
 
 // ------------------------------------------------------------------ decode page table
@@ -333,6 +472,28 @@ cudaError_t launch_page_table(const int32_t *sel, const int32_t *block_table, co
     k_page_table<<<unsigned((rows + 127) / 128), 128, 0, st>>>(sel, block_table, seq_lens, B, s.G, s.topk,
                                                                 s.max_blocks, n_pages, pt, row_len, err);
     return cudaGetLastError();
+}
+
+cudaError_t launch_decode_select(const float *scores, const int32_t *seq_lens, const int32_t *block_table,
+                                 int B, int n_pages, const Shape &s, int32_t *sel, int32_t *pt,
+                                 int32_t *row_len, int32_t *counters, int32_t *err, cudaStream_t st,
+                                 bool pdl) {
+    const int items = B * s.G;
+    if (items <= 0) return cudaSuccess;
+    const int mb = s.max_blocks;
+    const dim3 wgrid(unsigned((items + 7) / 8)), wblock(256);
+#define MSA_DSEL_ARGS scores, seq_lens, block_table, B, s.G, mb, s.topk, n_pages, sel, pt, row_len, counters, err
+    if (mb <= 128) return launch_kernel(k_decode_select_warp<4>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
+    if (mb <= 512) return launch_kernel(k_decode_select_warp<16>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
+    if (mb <= 1024) return launch_kernel(k_decode_select_warp<32>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
+    if (mb <= 8192)
+        return launch_kernel(k_decode_select_cta<256, 32>, dim3(unsigned(items)), dim3(256), 0, st, pdl,
+                             MSA_DSEL_ARGS);
+    if (mb <= 16384)
+        return launch_kernel(k_decode_select_cta<512, 32>, dim3(unsigned(items)), dim3(512), 0, st, pdl,
+                             MSA_DSEL_ARGS);
+#undef MSA_DSEL_ARGS
+    return cudaErrorNotSupported;
 }
 
 size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s) {

@@ -260,6 +260,39 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_attn_decode");
 }
 
+msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cache, const void *v_cache,
+                             const void *kidx_cache, const int32_t *block_table, const int32_t *seq_lens, int32_t B,
+                             int32_t n_pages, const msa_dims_t *dims, float *scores, int32_t *sel,
+                             int32_t *page_table, int32_t *row_len, void *out, float *lse, void *workspace,
+                             size_t workspace_bytes, int32_t *err_word, msa_stream_t stream) {
+    Shape s;
+    msa_status_t st = check_dims(dims, true, true, &s, "msa_decode_step");
+    if (st != MSA_OK) return st;
+    MSA_REQUIRE(B >= 0 && n_pages > 0, "msa_decode_step: bad sizes");
+    if (B == 0) return MSA_OK;
+    MSA_REQUIRE(q && q_idx && k_cache && v_cache && kidx_cache && block_table && seq_lens && scores && sel &&
+                    page_table && row_len && out && lse && err_word,
+                "msa_decode_step: NULL pointer");
+    if (1LL * B * s.G > 65535) return fail(MSA_ERR_UNSUPPORTED, "msa_decode_step: B*G > 65535");
+    if (s.max_blocks > 16384) return fail(MSA_ERR_UNSUPPORTED, "msa_decode_step: max_blocks > 16384");
+    const size_t need = decode_workspace_bytes(B, s);
+    if (!workspace || workspace_bytes < need)
+        return fail(MSA_ERR_WORKSPACE, "msa_decode_step: workspace needs %zu bytes", need);
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
+        return fail(MSA_ERR_INVALID_ARG, "msa_decode_step: caches must be 16-byte aligned");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_score_decode_seq(q_idx, kidx_cache, block_table, seq_lens, B, n_pages, s, scores,
+                                            err_word, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "msa_decode_step (index scan)");
+    int32_t *counters = decode_ws_counters(workspace, B, s);
+    e = launch_decode_select(scores, seq_lens, block_table, B, n_pages, s, sel, page_table, row_len, counters,
+                             err_word, cs, true);
+    if (e != cudaSuccess) return cuda_fail(e, "msa_decode_step (selection)");
+    e = launch_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, s, out, lse, workspace, err_word,
+                           cs, true, true);
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_decode_step (attention)");
+}
+
 size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_dims_t *dims) {
     Shape s;
     if (n_rows < 0) return 0;
@@ -306,6 +339,6 @@ const char *msa_status_str(msa_status_t status) {
 
 const char *msa_last_error(void) { return g_last_error; }
 
-int32_t msa_version(void) { return 100; }
+int32_t msa_version(void) { return 200; }
 
 }  // extern "C"

@@ -213,6 +213,18 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel on the stream is still running.  pdl_wait() blocks until that
+// kernel has completed and its memory is visible; everything the previous
+// kernel writes must be read after it.  pdl_trigger() lets the next kernel on
+// the stream start launching.  Both are no-ops for an ordinary launch.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -7,7 +7,28 @@
 
 #include "msa.h"
 
+#include <utility>
+
 namespace msa {
+
+// Launch `kernel` on `st`; with pdl == true the launch carries programmatic
+// stream serialisation, so it may overlap the tail of the previous kernel on the
+// stream (the kernel must call pdl_wait() before reading that kernel's output).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct Shape {
     int Hq, G, D, Di, topk, max_blocks, hpg;
@@ -47,11 +68,30 @@ cudaError_t launch_lse_merge(const void *o_part, const float *lse_part, const in
                              int n_rows, const Shape &s, void *out, float *lse, int32_t *err,
                              cudaStream_t st);
 
+// Decode workspace: split-by-page partials, their lse, and one merge counter per
+// (request, group) row.  The counters must be zero when the attention kernel
+// starts; launch_attn_decode clears them itself unless counters_zeroed is set
+// (the fused decode step clears them in its select kernel).
 size_t decode_workspace_bytes(int B, const Shape &s);
+int32_t *decode_ws_counters(void *ws, int B, const Shape &s);
 cudaError_t launch_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *pt, const int32_t *row_len, int B, int n_pages,
                                const Shape &s, void *out, float *lse, void *ws, int32_t *err,
-                               cudaStream_t st);
+                               cudaStream_t st, bool counters_zeroed = false, bool pdl = false);
+
+// Decode selection in one launch after the index scan: top-k per (request,
+// group), page table and row lengths; also zeroes `counters` (B*G entries,
+// may be null).  Launched with programmatic serialisation after the scan.
+cudaError_t launch_decode_select(const float *scores, const int32_t *seq_lens, const int32_t *block_table,
+                                 int B, int n_pages, const Shape &s, int32_t *sel, int32_t *pt,
+                                 int32_t *row_len, int32_t *counters, int32_t *err, cudaStream_t st,
+                                 bool pdl);
+
+// Decode index scan whose rows are the B requests themselves (row b is request
+// b at position seq_lens[b] - 1).
+cudaError_t launch_score_decode_seq(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                    const int32_t *seq_lens, int B, int n_pages, const Shape &s,
+                                    float *scores, int32_t *err, cudaStream_t st);
 
 // Tensor-map creation through the driver entry point (no libcuda link dependency).
 bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *dims,

@@ -12,9 +12,10 @@
 // The array exists once per GPU that loads the library and stays allocated until
 // the process exits.  Every call uses the same array, so calls whose kernels
 // overlap on the GPU (for example on two streams) race on it and must be
-// serialised by the caller.  The array keeps what the previous call left in it;
-// nothing in it has to start at zero, because the partial kernel writes every
-// lse slot and every partial that the merge then reads.
+// serialised by the caller.  The array keeps what the previous call left in it.
+// Only the per-row merge counters have to start at zero, and
+// msa_sparse_attn_decode clears them on the stream before its kernel runs; the
+// partials and their lse are written before they are read.
 #include <cuda_runtime.h>
 
 #include <cstdio>

@@ -123,7 +123,7 @@ msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const in
  *   scores fp32 [n_rows][G][max_blocks]
  *   q_pos  int32 [n_rows]
  *   sel    int32 [n_rows][G][topk]  out; ascending block ids, -1 padding
- * Candidate counts up to 32768 blocks (4M tokens) are supported.
+ * Candidate counts up to 16384 blocks (2M tokens) are supported.
  */
 msa_status_t msa_topk_blocks(const float *scores, const int32_t *q_pos, int32_t n_rows,
                              const msa_dims_t *dims, int32_t *sel, int32_t *err_word,
@@ -209,8 +209,10 @@ msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int3
  * tables ([T-zh 将 MSA 与分页注意力集成]): row r = b * G + g reads its row_len[r]
  * tokens from pages page_table[r][0], [1], ... in order (slot s holds tokens
  * s*128 .. s*128+127 of the row); the Hq/G heads of group g attend them.
- * Split by page: one partial per (row, slot) in the workspace, then an LSE
- * merge (the same reduction as msa_lse_merge).
+ * Split by page: one partial per (row, slot) in the workspace; the work item
+ * that finishes a row last merges the row's partials (the same reduction as
+ * msa_lse_merge), counted on a per-row counter in the workspace that this call
+ * clears before its kernel runs.
  *
  *   q          bf16 [B][Hq][D]
  *   page_table int32 [B*G][topk];  row_len int32 [B*G]
@@ -224,6 +226,32 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
                                     msa_stream_t stream);
 
 /*
+ * msa_decode_step -- one whole decode step for B requests, each with one new
+ * query token at position seq_lens[b] - 1: index scan (msa_index_score,
+ * MSA_PHASE_DECODE, rows = requests), top-k (msa_topk_blocks), page tables
+ * (msa_build_page_table) and paged sparse attention (msa_sparse_attn_decode),
+ * with the same results as those four calls.  [T-zh 解码索引评分内核优化,
+ * 将 MSA 与分页注意力集成]; [T-zh 未来工作]: the small top-k and page-table kernels
+ * are fused into one.  Three kernels run back to back with programmatic
+ * dependent launch, so each starts while the previous one drains.
+ *
+ *   q           bf16 [B][Hq][D];  q_idx bf16 [B][G][Di]
+ *   k_cache, v_cache bf16 [n_pages][128][G][D];  kidx_cache bf16 [n_pages][128][G][Di]
+ *   block_table int32 [B][max_blocks];  seq_lens int32 [B] (cached tokens incl. the new one)
+ *   scores      fp32 [B][G][max_blocks]  out
+ *   sel         int32 [B][G][topk]       out
+ *   page_table  int32 [B*G][topk], row_len int32 [B*G]  out
+ *   out         bf16 [B][Hq][D], lse fp32 [B][Hq]      out
+ *   workspace   msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims) bytes
+ * Limits: B*G <= 65535, max_blocks <= 16384; caches 16-byte aligned.
+ */
+msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cache, const void *v_cache,
+                             const void *kidx_cache, const int32_t *block_table, const int32_t *seq_lens, int32_t B,
+                             int32_t n_pages, const msa_dims_t *dims, float *scores, int32_t *sel,
+                             int32_t *page_table, int32_t *row_len, void *out, float *lse, void *workspace,
+                             size_t workspace_bytes, int32_t *err_word, msa_stream_t stream);
+
+/*
  * msa_sparse_attn_decode_noalloc -- the same computation as msa_sparse_attn_decode
  * for callers that cannot allocate device memory.  The pages have no counterpart
  * to it; it exists for callers like a serving engine that has reserved almost all
@@ -234,7 +262,7 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
  *
  *   Arguments, layouts and outputs: as msa_sparse_attn_decode, minus the workspace.
  *   Limit: msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims) must not exceed 16 MiB
- *   (for example B * G * topk <= 4064 rows x slots at Hq/G = 8, D = 128); larger
+ *   (for example B <= 31 requests at G = 8, topk = 16, Hq/G = 8, D = 128); larger
  *   calls return MSA_ERR_WORKSPACE and enqueue nothing.
  *   Allocation: none -- no cudaMalloc, cudaFree or allocating library routine.
  *   The array is static device memory that every GPU loading the library holds

@@ -101,7 +101,9 @@ def test_workspace_sizes_and_errors(lib):
     # bitmap over (group, block) keys x ceil(rows/32) words + per-key counts, 256-byte aligned
     assert inv == ((8 * 533 * 256 * 4 + 255) // 256) * 256 + ((8 * 533 * 4 + 255) // 256) * 256
     dec = lib.msa_workspace_bytes(1, 8, 0, ctypes.byref(good_dims()))
-    assert dec == ((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
+    # fp32 partials + their lse + one merge counter per (request, group) row, 256-byte aligned
+    assert dec == (((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
+                   + ((8 * 8 * 4 + 255) // 256) * 256)
     assert lib.msa_workspace_bytes(9, 8, 1, ctypes.byref(d)) == 0
     # too small a workspace is refused before any launch
     rc = lib.msa_invert_selection(FAKE, FAKE, 8192, 1, ctypes.byref(d), FAKE, FAKE, FAKE, ctypes.c_size_t(inv - 1),
@@ -110,6 +112,13 @@ def test_workspace_sizes_and_errors(lib):
     rc = lib.msa_sparse_attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 4096, ctypes.byref(good_dims()), FAKE, FAKE,
                                     FAKE, ctypes.c_size_t(dec - 1), FAKE, None)
     assert rc == 6
+    rc = lib.msa_decode_step(*([FAKE] * 7), 8, 4096, ctypes.byref(good_dims()), *([FAKE] * 6), FAKE,
+                             ctypes.c_size_t(dec - 1), FAKE, None)
+    assert rc == 6
+    # a scan over more than 16384 blocks is refused by the fused decode step
+    rc = lib.msa_decode_step(*([FAKE] * 7), 8, 4096, ctypes.byref(good_dims(max_blocks=16385)), *([FAKE] * 6),
+                             FAKE, ctypes.c_size_t(1 << 40), FAKE, None)
+    assert rc == 2
 
 
 def test_package_import_fails_loudly_without_library(tmp_path):

@@ -19,12 +19,23 @@ def msa():
 
 
 def _run_decode(m, case):
+    """The fused entry point msa_decode_step, and the same step through the four
+    separate entry points; both must give identical bits (same kernels for the
+    scan and attention, the same exact top-k rule)."""
     dims = m.dims_of(case)
     step = m.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
-    step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.seq_lens,
-         case.q_pos)
+    args = (case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.seq_lens,
+            case.q_pos)
+    step(*args)
     m.msa_check(step.err)
+    comp = m.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    comp.composed(*args)
+    m.msa_check(comp.err)
     torch.cuda.synchronize()
+    for name in ("scores", "sel", "page_table", "row_len", "out", "lse"):
+        a, b = getattr(step, name), getattr(comp, name)
+        assert torch.equal(a, b) or (name == "scores" and torch.equal(a.isneginf(), b.isneginf())
+                                     and torch.equal(a[~a.isneginf()], b[~b.isneginf()])), name
     return step
 
 
