@@ -24,6 +24,7 @@ MSA_PHASE_DECODE = 0
 MSA_PHASE_PREFILL = 1
 MSA_OP_INVERT = 0
 MSA_OP_DECODE = 1
+MSA_OP_PREFILL = 2
 
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
           4: "MSA_ERR_DEVICE_BOUNDS", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_WORKSPACE",
@@ -69,7 +70,7 @@ def _load() -> ctypes.CDLL:
         "msa_topk_blocks": [P, P, I, D, P, P, P],
         "msa_build_page_table": [P, P, P, I, I, D, P, P, P, P],
         "msa_invert_selection": [P, P, I, I, D, P, P, P, S, P, P],
-        "msa_sparse_attn_prefill": [P, P, P, P, P, P, P, P, I, I, I, D, P, P, P, P],
+        "msa_sparse_attn_prefill": [P, P, P, P, P, P, P, P, I, I, I, D, P, P, P, S, P, P],
         "msa_lse_merge": [P, P, P, I, D, P, P, P, P],
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
         "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
@@ -226,7 +227,7 @@ def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_e
 
 
 def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, dims: Dims,
-                            o_part=None, lse_part=None, err_word=None):
+                            o_part=None, lse_part=None, workspace=None, err_word=None):
     n_rows = q.shape[0]
     _req(q, torch.bfloat16, "q", (n_rows, dims.Hq, dims.D))
     _req(k_cache, torch.bfloat16, "k_cache")
@@ -246,11 +247,15 @@ def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_
         lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, device=dev)
     _req(o_part, torch.bfloat16, "o_part", (n_rows, dims.topk, dims.Hq, dims.D))
     _req(lse_part, torch.float32, "lse_part", (n_rows, dims.topk, dims.Hq))
+    need = msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    _req(workspace, torch.uint8, "workspace")
     err_word = new_err_word(dev) if err_word is None else err_word
     d = dims.c()
     _call("msa_sparse_attn_prefill", _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(q_req),
           _ptr(q_pos), _ptr(blk_off), _ptr(blk_ent), n_rows, n_req, k_cache.shape[0], ctypes.byref(d),
-          _ptr(o_part), _ptr(lse_part), _ptr(err_word), _stream(dev))
+          _ptr(o_part), _ptr(lse_part), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
     return o_part, lse_part
 
 
@@ -409,12 +414,14 @@ class PrefillStep:
         self.blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, **f)
         self.inv_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)),),
                                   dtype=torch.uint8, **f)
+        self.attn_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)),),
+                                   dtype=torch.uint8, **f)
         self.o_part = torch.empty((n_rows, dims.topk, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, **f)
         self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
         self.err = new_err_word(device)
-        self.kernel_launches = 9   # score, top-k, 4 inversion kernels (+ memset), attention, merge
+        self.kernel_launches = 10   # score, top-k, 4 inversion kernels (+ memset), plan, attention, merge
 
     def select(self, q_idx, kidx_cache, block_table, q_req, q_pos):
         msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
@@ -425,7 +432,7 @@ class PrefillStep:
 
     def attend(self, q, k_cache, v_cache, block_table, q_req, q_pos):
         msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, self.blk_off, self.blk_ent,
-                                self.dims, self.o_part, self.lse_part, err_word=self.err)
+                                self.dims, self.o_part, self.lse_part, self.attn_ws, err_word=self.err)
         return msa_lse_merge(self.o_part, self.lse_part, self.sel, self.dims, self.out, self.lse, err_word=self.err)
 
     def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, q_req, q_pos):

@@ -7,90 +7,174 @@
 // same operator property.  Each block yields a partial O per (query, head) that
 // is later combined by a Log-Sum-Exp reduction.
 //
-// One CTA owns one CSR key (KV group g, request, logical block j):
-//   warp 0     TMA: K_j and V_j once (4-D boxes of [128 tokens][64 dims],
-//              128B swizzle), then per tile of 128/HPG entries the HPG query
-//              heads of group g of each entry's query row (one 3-D box per entry
-//              and 64-column half) into a double-buffered Q tile;
-//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128 query-head rows,
-//              N = 128 tokens, K = D) into one of two TMEM S buffers, then
-//              O = P V (N = D, V used MN-major) into a TMEM O buffer; S of the
-//              next tile is issued before P of this one is ready;
-//   warps 2-5  thread = query-head row: tcgen05.ld of S, causal mask against the
-//              entry's position, exp2 softmax, P as bf16 into shared memory for
-//              the second MMA, then tcgen05.ld of O, normalisation, bf16 store of
-//              the partial and its lse.
-// All waits are bounded; a timeout raises MSA_FLAG_TIMEOUT and drains.
+// Work.  A CSR key (KV group g, request, logical block j) lists the (query,
+// slot) entries that selected block j.  A tile is 128/HPG consecutive entries of
+// one key times the HPG query heads of group g = 128 rows of the tensor-core M
+// dimension.  A plan kernel cuts every key into chunks of at most kChunkTiles
+// tiles; the attention kernel runs one persistent CTA per SM that takes chunks
+// from an atomic counter in key order, so a block selected by thousands of
+// queries is spread over many SMs while its K/V stays in L2.
+//
+// One CTA (10 warps):
+//   warp 0     producer: per chunk, K_j and V_j by TMA (128B swizzle, 64-column
+//              boxes) into one of two K/V buffers; per tile, decodes the entries
+//              (query row, slot, causal limit) into a ring of tile descriptors and
+//              gathers the HPG heads of each entry's query row by TMA into one of
+//              two Q buffers;
+//   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
+//              K = D) into the S buffer of the tile's softmax group, then, once P
+//              is back in TMEM, O = P V with P as the TMEM A operand and V as an
+//              MN-major shared-memory B operand;
+//   warps 2-5, 6-9  two softmax groups that take alternate tiles: tcgen05.ld of
+//              S (thread = row), causal mask, exp2 softmax, P as packed bf16
+//              written over S (tcgen05.st), then tcgen05.ld of O, normalisation,
+//              bf16 partial and lse stores.  While one group runs its softmax
+//              the tensor core works on the other group's tile.
+// TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D of 512 columns).
+// Every wait is bounded; a timeout raises MSA_FLAG_TIMEOUT and every role drains.
 #include "msa_device.cuh"
 #include "msa_internal.h"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kChunkTiles = 8;   // tiles per work chunk
+constexpr int kRing = 4;         // tile descriptors in flight
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr int kFlagKv1 = 1;      // K/V buffer 1 (else 0)
+constexpr int kFlagFirst = 2;    // first tile of its chunk
+constexpr int kFlagLast = 4;     // last tile of its chunk
+constexpr int kFlagEnd = 8;      // no more work
+
+struct TileDesc {
+    int32_t flags;
+    int32_t g;
+    int32_t qq[32];    // query row of each entry, -1 for padding / rejected entries
+    int32_t slot[32];  // selection slot of the entry
+    int32_t lim[32];   // tokens t <= lim of the block are visible to the entry
+};
+
 template <int D>
 struct AttnSmem {
-    alignas(1024) uint8_t k[D * 128 * 2];
-    alignas(1024) uint8_t v[D * 128 * 2];
+    alignas(1024) uint8_t k[2][D * 128 * 2];
+    alignas(1024) uint8_t v[2][D * 128 * 2];
     alignas(1024) uint8_t q[2][128 * D * 2];
-    alignas(1024) uint8_t p[128 * 128 * 2];
-    uint64_t kv_full;
+    TileDesc desc[kRing];
+    uint64_t kv_full[2], kv_empty[2];
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, o_full, o_free;
+    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t desc_full[kRing], desc_empty[kRing];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+
+// Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
+constexpr size_t kPlanHeaderBytes = 16;
+
+__host__ __device__ inline long long max_chunks_of(long long n_keys, long long n_entries, int ept) {
+    const long long per_chunk = static_cast<long long>(ept) * kChunkTiles;
+    return n_keys + (n_entries + per_chunk - 1) / per_chunk;
+}
+
+// ------------------------------------------------------------------ plan
+//
+// One CTA: chunk counts per key (ceil(ceil(n/EPT)/kChunkTiles)), an exclusive
+// scan, and the chunk list {key, first tile} in key order.
+__global__ void __launch_bounds__(1024) k_attn_plan(const int32_t *__restrict__ blk_off, int n_keys, int ept,
+                                                    long long max_chunks, int32_t *__restrict__ hdr,
+                                                    int2 *__restrict__ chunks, int32_t *err) {
+    __shared__ int32_t wsum[32];
+    __shared__ long long carry_s;
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry_s = 0;
+    __syncthreads();
+    for (int base = 0; base < n_keys; base += 1024) {
+        const int k = base + tid;
+        int nc = 0;
+        if (k < n_keys) {
+            const int n = blk_off[k + 1] - blk_off[k];
+            if (n < 0) {
+                raise_flag(err, MSA_FLAG_BOUNDS);
+            } else {
+                const int nt = (n + ept - 1) / ept;
+                nc = (nt + kChunkTiles - 1) / kChunkTiles;
+            }
+        }
+        int x = nc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const long long start = carry_s + (warp ? wsum[warp - 1] : 0) + x - nc;
+        for (int i = 0; i < nc; ++i) {
+            if (start + i < max_chunks) chunks[start + i] = make_int2(k, i * kChunkTiles);
+            else raise_flag(err, MSA_FLAG_BOUNDS);
+        }
+        __syncthreads();
+        if (tid == 1023) carry_s = start + nc;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        hdr[0] = 0;
+        hdr[1] = int32_t(carry_s < max_chunks ? carry_s : max_chunks);
+    }
+}
+
+// ------------------------------------------------------------------ attention
 
 template <int D, int HPG>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const int32_t *__restrict__ block_table,
     const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos, const int32_t *__restrict__ blk_off,
-    const int32_t *__restrict__ blk_ent, int n_rows, int n_req, int n_pages, int G, int topk, int max_blocks,
-    float sm_scale, uint16_t *__restrict__ o_part, float *__restrict__ lse_part, int32_t *err) {
+    const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr, const int2 *__restrict__ chunks,
+    int n_rows, int n_req, int n_pages, int G, int topk, int max_blocks, float sm_scale,
+    uint16_t *__restrict__ o_part, float *__restrict__ lse_part, int32_t *err) {
     constexpr int EPT = 128 / HPG;                 // entries per tile
     constexpr int NSUB = D / 64;                   // 64-column sub-tiles
     constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t kIdescO = make_idesc_bf16(128, D, 0, 1);
-    constexpr uint32_t kTmemO = 256;
     extern __shared__ uint8_t smem_raw[];
     AttnSmem<D> &sm =
         *reinterpret_cast<AttnSmem<D> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int key = blockIdx.x;
-    const int off = blk_off[key];
-    const int end = blk_off[key + 1];
-    if (end <= off) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long cap = 1LL * n_rows * G * topk;
-    const int per_g = n_req * max_blocks;
-    const int g = key / per_g;
-    const int req = (key - g * per_g) / max_blocks;
-    const int j = key - g * per_g - req * max_blocks;
-    int page = block_table[size_t(req) * max_blocks + j];
-    if (off < 0 || end > cap || page < 0 || page >= n_pages) {
-        if (tid == 0) raise_flag(err, MSA_FLAG_BOUNDS);
-        return;
-    }
-    const int n_ent = end - off;
-    const int n_tiles = (n_ent + EPT - 1) / EPT;
+    const int Hq = G * HPG;
 
     if (tid == 0) {
-        mbar_init(&sm.kv_full, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.kv_full[b], 1);
+            mbar_init(&sm.kv_empty[b], 1);
             mbar_init(&sm.q_full[b], 1);
             mbar_init(&sm.q_empty[b], 1);
             mbar_init(&sm.s_full[b], 1);
-            mbar_init(&sm.s_free[b], 4);
+            mbar_init(&sm.p_full[b], 4);
+            mbar_init(&sm.o_full[b], 1);
+            mbar_init(&sm.o_free[b], 4);
         }
-        mbar_init(&sm.p_full, 4);
-        mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.o_free, 4);
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(&sm.desc_full[r], 32);
+            mbar_init(&sm.desc_empty[r], 5);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
         fence_mbar_init();
@@ -99,51 +183,188 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         tmem_alloc(&sm.tmem_base, 512);
         tmem_relinquish();
     }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) {
-            tma_prefetch_desc(&qmap);
-            mbar_arrive_expect_tx(&sm.kv_full, 2 * D * 128 * 2);
+        // ------------------------------------------------------------ producer
+        pdl_wait();   // the work list and the CSR come from the preceding kernels
+        const int n_chunks = plan_hdr[1];
+        const int per_g = n_req * max_blocks;
+        int u = 0;          // tiles described
+        int n_q = 0;        // tiles whose Q copies were issued
+        int cs = 0;         // chunks whose K/V were loaded
+        bool ok = true;
+        int c = 0;
+        if (lane == 0) c = atomicAdd(plan_hdr, 1);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        while (ok && c < n_chunks) {
+            int cn = 0;
+            if (lane == 0) cn = atomicAdd(plan_hdr, 1);
+            cn = __shfl_sync(0xffffffffu, cn, 0);
+            const int2 ch = chunks[c];
+            const int key = ch.x, t0 = ch.y;
+            const int g = key / per_g;
+            const int req = (key - g * per_g) / max_blocks;
+            const int j = key - g * per_g - req * max_blocks;
+            const int off0 = blk_off[key], end0 = blk_off[key + 1];
+            const int page = block_table[size_t(req) * max_blocks + j];
+            if (off0 < 0 || end0 > cap || off0 > end0 || page < 0 || page >= n_pages || g >= G) {
+                if (lane == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+                c = cn;
+                continue;
+            }
+            const int off = off0 + t0 * EPT;
+            const int end = min(end0, off + kChunkTiles * EPT);
+            if (off >= end) {
+                c = cn;
+                continue;
+            }
+            const int nt = (end - off + EPT - 1) / EPT;
+            const int kvb = cs & 1;
+            if (cs >= 2) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait(&sm.kv_empty[kvb], ((cs >> 1) - 1) & 1, err, &sm.abort);
+                if (!__shfl_sync(0xffffffffu, w, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sm.kv_full[kvb], 2 * D * 128 * 2);
 #pragma unroll
-            for (int i = 0; i < NSUB; ++i) tma_load_4d(sm.k + i * 16384, &kmap, &sm.kv_full, i * 64, g, 0, page);
+                for (int i = 0; i < NSUB; ++i)
+                    tma_load_4d(sm.k[kvb] + i * 16384, &kmap, &sm.kv_full[kvb], i * 64, g, 0, page);
 #pragma unroll
-            for (int i = 0; i < NSUB; ++i) tma_load_4d(sm.v + i * 16384, &vmap, &sm.kv_full, i * 64, g, 0, page);
-            int issued = 0;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int b = t & 1;
-                if (t >= 2 && !mbar_wait(&sm.q_empty[b], ((t >> 1) - 1) & 1, err, &sm.abort)) break;
-                mbar_arrive_expect_tx(&sm.q_full[b], 128 * D * 2);
-                for (int e = 0; e < EPT; ++e) {
-                    const int idx = off + t * EPT + e;
-                    int qq = n_rows;                    // fully out of bounds -> zero rows
-                    if (idx < end) {
-                        const int v = blk_ent[idx] / topk;
-                        if (v >= 0 && v < n_rows) qq = v;
+                for (int i = 0; i < NSUB; ++i)
+                    tma_load_4d(sm.v[kvb] + i * 16384, &vmap, &sm.kv_full[kvb], i * 64, g, 0, page);
+            }
+            ++cs;
+            for (int t = 0; t < nt; ++t) {
+                const int slot = u % kRing, qb = u & 1;
+                if (u >= kRing) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait(&sm.desc_empty[slot], ((u / kRing) - 1) & 1, err, &sm.abort);
+                    if (!__shfl_sync(0xffffffffu, w, 0)) {
+                        ok = false;
+                        break;
                     }
+                }
+                TileDesc &d = sm.desc[slot];
+                int qq = -1;
+                if (lane < EPT) {
+                    const int idx = off + t * EPT + lane;
+                    int sl = 0, lim = -1;
+                    if (idx < end) {
+                        const int ent = blk_ent[idx];
+                        const int v = ent / topk;
+                        if (ent < 0 || v >= n_rows || q_req[v] != req) {
+                            raise_flag(err, MSA_FLAG_BOUNDS);
+                        } else {
+                            lim = q_pos[v] - j * 128;
+                            if (lim < 0) {   // block past the row's position: not a candidate
+                                raise_flag(err, MSA_FLAG_BOUNDS);
+                            } else {
+                                qq = v;
+                                sl = ent - v * topk;
+                            }
+                        }
+                    }
+                    d.qq[lane] = qq;
+                    d.slot[lane] = sl;
+                    d.lim[lane] = lim;
+                }
+                if (u >= 2) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((u >> 1) - 1) & 1, err, &sm.abort);
+                    if (!__shfl_sync(0xffffffffu, w, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    d.flags = (kvb ? kFlagKv1 : 0) | (t == 0 ? kFlagFirst : 0) | (t == nt - 1 ? kFlagLast : 0);
+                    d.g = g;
+                    mbar_arrive_expect_tx(&sm.q_full[qb], 128 * D * 2);
+                }
+                __syncwarp();
+                if (lane < EPT) {
+                    const int row = qq >= 0 ? qq : n_rows;   // fully out of bounds -> zero rows
 #pragma unroll
                     for (int i = 0; i < NSUB; ++i)
-                        tma_load_3d(sm.q[b] + i * 16384 + e * HPG * 128, &qmap, &sm.q_full[b], i * 64, g * HPG, qq);
+                        tma_load_3d(sm.q[qb] + i * 16384 + lane * HPG * 128, &qmap, &sm.q_full[qb], i * 64,
+                                    g * HPG, row);
                 }
-                issued = t + 1;
+                mbar_arrive(&sm.desc_full[slot]);
+                ++u;
+                n_q = u;
             }
-            if (sm.abort) {
-                mbar_wait(&sm.kv_full, 0, err, nullptr);
-                for (int t = max(0, issued - 2); t < issued; ++t) mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, err, nullptr);
+            c = cn;
+        }
+        // two end markers, one for each softmax group (the MMA warp stops at the first)
+        for (int e = 0; ok && e < 2; ++e) {
+            const int slot = u % kRing;
+            if (u >= kRing) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait(&sm.desc_empty[slot], ((u / kRing) - 1) & 1, err, &sm.abort);
+                if (!__shfl_sync(0xffffffffu, w, 0)) break;
             }
+            if (lane == 0) sm.desc[slot].flags = kFlagEnd;
+            __syncwarp();
+            mbar_arrive(&sm.desc_full[slot]);
+            ++u;
+        }
+        if (sm.abort && lane == 0) {
+            // drain: the copies still in flight land before the CTA exits (u counts the two end
+            // markers only when the loop finished; tiles before them issued their Q copies)
+            for (int t = max(0, cs - 2); t < cs; ++t) mbar_wait(&sm.kv_full[t & 1], (t >> 1) & 1, err, nullptr);
+            for (int t = max(0, n_q - 2); t < n_q; ++t) mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, err, nullptr);
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v), p_addr = smem_u32(sm.p);
-            auto issue_s = [&](int t) -> bool {
+            int u = 0, cs = -1;
+            bool have_prev = false;
+            int p_u = 0, p_flags = 0;
+            auto do_pv = [&](int t, int flags) -> bool {
                 const int b = t & 1;
-                if (!mbar_wait(&sm.q_full[b], (t >> 1) & 1, err, &sm.abort)) return false;
-                if (t >= 2 && !mbar_wait(&sm.s_free[b], ((t >> 1) - 1) & 1, err, &sm.abort)) return false;
+                if (!mbar_wait(&sm.p_full[b], (t >> 1) & 1, err, &sm.abort)) return false;
+                if (t >= 2 && !mbar_wait(&sm.o_free[b], ((t >> 1) - 1) & 1, err, &sm.abort)) return false;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(sm.q[b]);
+                const int kvb = flags & kFlagKv1;
+                const uint32_t v_addr = smem_u32(sm.v[kvb]);
+#pragma unroll
+                for (int kt = 0; kt < 8; ++kt) {
+                    const uint64_t bd = make_smem_desc(v_addr + uint32_t(kt * 2048), 16384, 1024, 2);
+                    mma_bf16_ts(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128 + kt * 8), bd, kIdescO,
+                                kt > 0 ? 1u : 0u);
+                }
+                mma_commit(&sm.o_full[b]);
+                if (flags & kFlagLast) mma_commit(&sm.kv_empty[kvb]);
+                return true;
+            };
+            for (;;) {
+                const int slot = u % kRing;
+                if (!mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort)) break;
+                const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
+                if (flags & kFlagEnd) break;
+                mbar_arrive(&sm.desc_empty[slot]);
+                const int kvb = flags & kFlagKv1;
+                if (flags & kFlagFirst) {
+                    ++cs;
+                    if (!mbar_wait(&sm.kv_full[kvb], (cs >> 1) & 1, err, &sm.abort)) break;
+                }
+                const int b = u & 1;
+                if (!mbar_wait(&sm.q_full[b], (u >> 1) & 1, err, &sm.abort)) break;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(sm.q[b]), k_addr = smem_u32(sm.k[kvb]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = uint32_t((kk >> 2) * 16384 + (kk & 3) * 32);
@@ -152,122 +373,114 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 }
                 mma_commit(&sm.s_full[b]);
                 mma_commit(&sm.q_empty[b]);
-                return true;
-            };
-            bool ok = mbar_wait(&sm.kv_full, 0, err, &sm.abort) && issue_s(0);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                if (t + 1 < n_tiles && !issue_s(t + 1)) break;
-                if (!mbar_wait(&sm.p_full, t & 1, err, &sm.abort)) break;
-                if (t >= 1 && !mbar_wait(&sm.o_free, (t - 1) & 1, err, &sm.abort)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kt = 0; kt < 8; ++kt) {
-                    const uint64_t ad = make_smem_desc(p_addr + uint32_t((kt >> 2) * 16384 + (kt & 3) * 32), 16, 1024, 2);
-                    const uint64_t bd = make_smem_desc(v_addr + uint32_t(kt * 2048), 16384, 1024, 2);
-                    mma_bf16(tmem + kTmemO, ad, bd, kIdescO, kt > 0 ? 1u : 0u);
+                if (have_prev && !do_pv(p_u, p_flags)) {
+                    have_prev = false;
+                    break;
                 }
-                mma_commit(&sm.o_full);
+                have_prev = true;
+                p_u = u;
+                p_flags = flags;
+                ++u;
             }
+            if (have_prev && !sm.abort) do_pv(p_u, p_flags);
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
     } else {
-        const int quad = warp & 3;
+        // ------------------------------------------------------------ softmax groups
+        const int wg = (warp - 2) >> 2;
+        const int quad = warp & 3;                 // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const int e = row / HPG, h = row - (row / HPG) * HPG;
-        const uint32_t lane_addr = tmem + (uint32_t(quad * 32) << 16);
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        const uint32_t t_s = tmem + lane_off + uint32_t(wg * 128);
+        const uint32_t t_o = tmem + lane_off + uint32_t(256 + wg * D);
         const float scale = sm_scale * kLog2e;
-        const uint32_t p_row = smem_u32(sm.p) + uint32_t(row * 128);
-        for (int t = 0; t < n_tiles; ++t) {
-            const int b = t & 1;
-            const int idx = off + t * EPT + e;
-            bool valid = idx < end;
-            int qq = 0, slot = 0, lim = 127;
-            if (valid) {
-                const int ent = blk_ent[idx];
-                qq = ent / topk;
-                slot = ent - qq * topk;
-                if (ent < 0 || qq >= n_rows || q_req[qq] != req) {
-                    raise_flag(err, MSA_FLAG_BOUNDS);
-                    valid = false;
-                } else {
-                    lim = q_pos[qq] - j * 128;
-                    if (lim < 0) {                      // block past the row's position: not a candidate
-                        raise_flag(err, MSA_FLAG_BOUNDS);
-                        valid = false;
-                        lim = 127;
-                    }
-                }
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[b], (t >> 1) & 1, err, &sm.abort))) break;
+        for (int u = wg;; u += 2) {
+            const int slot = u % kRing;
+            const int k = u >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort))) break;
+            const volatile TileDesc &d = sm.desc[slot];
+            if (d.flags & kFlagEnd) break;
+            const int g = d.g;
+            const int qq = d.qq[e], sl = d.slot[e];
+            const int lim = qq >= 0 ? d.lim[e] : 127;   // padding rows: any finite softmax, never stored
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.desc_empty[slot]);
+
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
             float s[128];
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + uint32_t(b * 128 + c0), v);
+                tmem_ld32(t_s + uint32_t(c0), v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(v[i]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.s_free[b]);
             float m = -INFINITY;
+            if (lim >= 127) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                s[c] = (c <= lim) ? s[c] * scale : -INFINITY;
-                m = fmaxf(m, s[c]);
+                for (int c = 0; c < 128; ++c) m = fmaxf(m, s[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    s[c] = c <= lim ? s[c] : -INFINITY;
+                    m = fmaxf(m, s[c]);
+                }
             }
+            const float ms = m * scale;
             // l: sum of the bf16-rounded probabilities the PV MMA consumes (normalises O);
             // le: exact fp32 sum (gives the lse)
             float l = 0.f, le = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 8) {
-                uint32_t w[4];
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                uint32_t w[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float pa = exp2f(s[c0 + 2 * i] - m), pb = exp2f(s[c0 + 2 * i + 1] - m);
+                for (int i = 0; i < 32; ++i) {
+                    const float pa = exp2f(fmaf(s[c0 + 2 * i], scale, -ms));
+                    const float pb = exp2f(fmaf(s[c0 + 2 * i + 1], scale, -ms));
                     w[i] = pack_bf16x2(pa, pb);
                     l += bf16_lo(w[i]) + bf16_hi(w[i]);
                     le += pa + pb;
                 }
-                const int cc = (c0 & 63) >> 3;
-                const uint32_t addr = p_row + uint32_t((c0 >> 6) * 16384) + uint32_t((cc ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
+                tmem_st32(t_s + uint32_t(c0 >> 1), w);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full);
+            if (lane == 0) mbar_arrive(&sm.p_full[wg]);
 
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full, t & 1, err, &sm.abort))) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
-            const float inv = 1.0f / l;
-            uint16_t *dst = o_part + ((size_t(qq) * topk + slot) * (size_t(G) * HPG) + size_t(g) * HPG + h) * D;
+            uint32_t ov[D];
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
-                tmem_ld32(lane_addr + kTmemO + uint32_t(c0), v);
+                tmem_ld32(t_o + uint32_t(c0), v);
                 tmem_ld_wait();
-                if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[i + 0]) * inv, __uint_as_float(v[i + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + c0 + i) = w;
-                    }
-                }
+                for (int i = 0; i < 32; ++i) ov[c0 + i] = v[i];
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.o_free);
-            if (valid)
-                lse_part[(size_t(qq) * topk + slot) * (size_t(G) * HPG) + size_t(g) * HPG + h] = (m + log2f(le)) * kLn2;
+            if (lane == 0) mbar_arrive(&sm.o_free[wg]);
+            if (qq >= 0) {
+                const float inv = 1.0f / l;
+                const size_t unit = (size_t(qq) * topk + sl) * size_t(Hq) + size_t(g) * HPG + h;
+                uint16_t *dst = o_part + unit * D;
+#pragma unroll
+                for (int i = 0; i < D; i += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[i + 0]) * inv, __uint_as_float(ov[i + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(dst + i) = w;
+                }
+                lse_part[unit] = (ms + log2f(le)) * kLn2;
+            }
         }
     }
 
@@ -277,10 +490,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+struct PlanLayout {
+    long long max_chunks;
+    size_t bytes;
+};
+
+inline PlanLayout plan_layout(int n_rows, int n_req, const Shape &s) {
+    const long long n_keys = 1LL * s.G * n_req * s.max_blocks;
+    const long long n_ent = 1LL * n_rows * s.G * s.topk;
+    PlanLayout p;
+    p.max_chunks = max_chunks_of(n_keys, n_ent, 128 / s.hpg);
+    p.bytes = kPlanHeaderBytes + size_t(p.max_chunks) * sizeof(int2);
+    return p;
+}
+
 template <int D, int HPG>
 cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, const int32_t *bt, const int32_t *q_req,
                      const int32_t *q_pos, const int32_t *blk_off, const int32_t *blk_ent, int n_rows, int n_req,
-                     int n_pages, const Shape &s, void *o_part, float *lse_part, int32_t *err, cudaStream_t st) {
+                     int n_pages, const Shape &s, void *o_part, float *lse_part, void *ws, int32_t *err,
+                     cudaStream_t st) {
     alignas(64) CUtensorMap qm, km, vm;
     const char *why = nullptr;
     {
@@ -297,27 +525,34 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
         if (!encode_tensor_map(&vm, 4, v_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
     }
     const long long n_keys = 1LL * s.G * n_req * s.max_blocks;
-    if (n_keys > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const size_t smem = sizeof(AttnSmem<D>) + 1024;
-    cudaError_t e =
-        cudaFuncSetAttribute(k_attn_prefill<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (n_keys > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
+    const PlanLayout pl = plan_layout(n_rows, n_req, s);
+    int32_t *hdr = static_cast<int32_t *>(ws);
+    int2 *chunks = reinterpret_cast<int2 *>(static_cast<uint8_t *>(ws) + kPlanHeaderBytes);
+    cudaError_t e = launch_kernel(k_attn_plan, dim3(1), dim3(1024), 0, st, false, blk_off, int(n_keys), 128 / HPG,
+                                  pl.max_chunks, hdr, chunks, err);
     if (e != cudaSuccess) return e;
-    k_attn_prefill<D, HPG><<<unsigned(n_keys), kThreads, smem, st>>>(
-        qm, km, vm, bt, q_req, q_pos, blk_off, blk_ent, n_rows, n_req, n_pages, s.G, s.topk, s.max_blocks,
-        s.sm_scale, static_cast<uint16_t *>(o_part), lse_part, err);
-    return cudaGetLastError();
+    const size_t smem = sizeof(AttnSmem<D>) + 1024;
+    e = cudaFuncSetAttribute(k_attn_prefill<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true, qm, km,
+                         vm, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows, n_req,
+                         n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, static_cast<uint16_t *>(o_part), lse_part,
+                         err);
 }
 
 }  // namespace
 
+size_t prefill_workspace_bytes(int n_rows, int n_req, const Shape &s) { return plan_layout(n_rows, n_req, s).bytes; }
+
 cudaError_t launch_attn_prefill(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
                                 const int32_t *q_req, const int32_t *q_pos, const int32_t *blk_off,
                                 const int32_t *blk_ent, int n_rows, int n_req, int n_pages, const Shape &s,
-                                void *o_part, float *lse_part, int32_t *err, cudaStream_t st) {
+                                void *o_part, float *lse_part, void *ws, int32_t *err, cudaStream_t st) {
 #define MSA_AP_CASE(DD, HH)                                                                                  \
     if (s.D == DD && s.hpg == HH)                                                                            \
         return launch_t<DD, HH>(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, n_rows, n_req, \
-                                n_pages, s, o_part, lse_part, err, st);
+                                n_pages, s, o_part, lse_part, ws, err, st);
     MSA_AP_CASE(128, 8) MSA_AP_CASE(128, 4) MSA_AP_CASE(64, 8) MSA_AP_CASE(64, 4)
 #undef MSA_AP_CASE
     return cudaErrorNotSupported;

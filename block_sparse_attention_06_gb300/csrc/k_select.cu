@@ -27,26 +27,39 @@ __device__ __forceinline__ uint64_t block_key(float s, int j, int32_t *err) {
 
 __device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
+// Largest of a lane's keys that is below `bound` (0 when none): four independent
+// max chains, so the dependent depth is PER/4 + 2 instead of PER.
+template <int PER>
+__device__ __forceinline__ uint64_t lane_max_below(const uint64_t (&keys)[PER], uint64_t bound) {
+    uint64_t part[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const uint64_t k = keys[i] < bound ? keys[i] : 0ull;
+        part[i & 3] = max_u64(part[i & 3], k);
+    }
+    return max_u64(max_u64(part[0], part[1]), max_u64(part[2], part[3]));
+}
+
 // The n best keys (n <= 32) among a warp's candidate keys, best first: lane i < n
 // receives the i-th best key, every other lane 0.  A key of 0 is "no candidate";
-// when fewer than n candidates exist the missing ranks are 0 too.  Each round
-// takes the largest key below the previous round's, so equal scores are ordered
-// by the block id inside the key and nothing is picked twice.
+// when fewer than n candidates exist the missing ranks are 0 too.  Every lane
+// keeps its best key not yet taken; a round takes the warp maximum of those
+// (two 32-bit warp reductions: score word, then block word among the lanes that
+// hold that score) and only the lane it came from moves to its next key.  Keys
+// are unique (the block id is inside), so equal scores are ordered by block id
+// and nothing is taken twice.
 template <int PER>
 __device__ __forceinline__ uint64_t warp_top_n(const uint64_t (&keys)[PER], int n) {
     const int lane = threadIdx.x & 31;
-    uint64_t prev = ~0ull, mine = 0;
+    uint64_t local = lane_max_below<PER>(keys, ~0ull);
+    uint64_t mine = 0;
     for (int round = 0; round < n; ++round) {
-        uint64_t best = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const uint64_t k = keys[i];
-            best = (k < prev && k > best) ? k : best;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = max_u64(best, __shfl_xor_sync(0xffffffffu, best, o));
-        prev = best;
+        const uint32_t hi = uint32_t(local >> 32);
+        const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+        const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? uint32_t(local) : 0u);
+        const uint64_t best = (uint64_t(mhi) << 32) | mlo;
         if (lane == round) mine = best;
+        if (best != 0ull && local == best) local = lane_max_below<PER>(keys, best);
     }
     return mine;
 }
@@ -55,9 +68,10 @@ __device__ __forceinline__ uint64_t warp_top_n(const uint64_t (&keys)[PER], int 
 // (ascending order); only meaningful for lanes < n.
 __device__ __forceinline__ int rank_ascending(int id, int n) {
     int rank = 0;
-    for (int l = 0; l < n; ++l) {
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
         const int other = __shfl_sync(0xffffffffu, id, l);
-        rank += other < id ? 1 : 0;
+        rank += (l < n && other < id) ? 1 : 0;
     }
     return rank;
 }

@@ -209,7 +209,8 @@ msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const v
                                      const int32_t *block_table, const int32_t *q_req, const int32_t *q_pos,
                                      const int32_t *blk_off, const int32_t *blk_ent, int32_t n_rows, int32_t n_req,
                                      int32_t n_pages, const msa_dims_t *dims, void *o_part, float *lse_part,
-                                     int32_t *err_word, msa_stream_t stream) {
+                                     void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                     msa_stream_t stream) {
     Shape s;
     msa_status_t st = check_dims(dims, true, false, &s, "msa_sparse_attn_prefill");
     if (st != MSA_OK) return st;
@@ -218,8 +219,15 @@ msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const v
     MSA_REQUIRE(q && k_cache && v_cache && block_table && q_req && q_pos && blk_off && blk_ent && o_part &&
                     lse_part && err_word,
                 "msa_sparse_attn_prefill: NULL pointer");
+    if (1.0 * n_rows * s.G * s.topk > 2147483647.0)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_prefill: more than 2^31 entries");
+    const size_t need = prefill_workspace_bytes(n_rows, n_req, s);
+    if (!workspace || workspace_bytes < need)
+        return fail(MSA_ERR_WORKSPACE, "msa_sparse_attn_prefill: workspace needs %zu bytes", need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+        return fail(MSA_ERR_INVALID_ARG, "msa_sparse_attn_prefill: workspace must be 16-byte aligned");
     cudaError_t e = launch_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, n_rows,
-                                        n_req, n_pages, s, o_part, lse_part, err_word,
+                                        n_req, n_pages, s, o_part, lse_part, workspace, err_word,
                                         static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_attn_prefill");
 }
@@ -303,6 +311,10 @@ size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_
     if (op == MSA_OP_DECODE) {
         if (check_dims(dims, true, false, &s, "msa_workspace_bytes") != MSA_OK) return 0;
         return decode_workspace_bytes(n_rows, s);
+    }
+    if (op == MSA_OP_PREFILL) {
+        if (check_dims(dims, true, false, &s, "msa_workspace_bytes") != MSA_OK || n_req <= 0) return 0;
+        return prefill_workspace_bytes(n_rows, n_req, s);
     }
     return 0;
 }

@@ -57,12 +57,15 @@ cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, 
                           const Shape &s, int32_t *blk_off, int32_t *blk_ent, void *ws,
                           int32_t *err, cudaStream_t st);
 
+// Block-major prefill attention: a plan kernel writes the chunk work list into
+// the workspace, then one persistent CTA per SM consumes it.
+size_t prefill_workspace_bytes(int n_rows, int n_req, const Shape &s);
 cudaError_t launch_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                                 const int32_t *block_table, const int32_t *q_req,
                                 const int32_t *q_pos, const int32_t *blk_off,
                                 const int32_t *blk_ent, int n_rows, int n_req, int n_pages,
-                                const Shape &s, void *o_part, float *lse_part, int32_t *err,
-                                cudaStream_t st);
+                                const Shape &s, void *o_part, float *lse_part, void *ws,
+                                int32_t *err, cudaStream_t st);
 
 cudaError_t launch_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel,
                              int n_rows, const Shape &s, void *out, float *lse, int32_t *err,

@@ -84,8 +84,9 @@ typedef void *msa_stream_t;
 #define MSA_PHASE_PREFILL 1
 
 /* Operation selector of msa_workspace_bytes. */
-#define MSA_OP_INVERT 0
-#define MSA_OP_DECODE 1
+#define MSA_OP_INVERT  0
+#define MSA_OP_DECODE  1
+#define MSA_OP_PREFILL 2
 
 /*
  * msa_index_score -- block scores for every (row, group, candidate block).
@@ -180,13 +181,18 @@ msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int3
  *   blk_off, blk_ent  the CSR of msa_invert_selection (same n_req, dims)
  *   o_part   bf16 [n_rows][topk][Hq][D]  out
  *   lse_part fp32 [n_rows][topk][Hq]     out
+ *   workspace device scratch of msa_workspace_bytes(MSA_OP_PREFILL, n_rows,
+ *            n_req, ...) bytes, 16-byte aligned: the work list (each key cut
+ *            into chunks of at most 8 tiles of 128/(Hq/G) entries) that one
+ *            persistent CTA per SM consumes; written by the call itself.
  */
 msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                                      const int32_t *block_table, const int32_t *q_req,
                                      const int32_t *q_pos, const int32_t *blk_off,
                                      const int32_t *blk_ent, int32_t n_rows, int32_t n_req,
                                      int32_t n_pages, const msa_dims_t *dims, void *o_part,
-                                     float *lse_part, int32_t *err_word, msa_stream_t stream);
+                                     float *lse_part, void *workspace, size_t workspace_bytes,
+                                     int32_t *err_word, msa_stream_t stream);
 
 /*
  * msa_lse_merge -- Log-Sum-Exp reduction of per-block partials.  [T-zh KV
@@ -281,7 +287,8 @@ msa_status_t msa_sparse_attn_decode_noalloc(const void *q, const void *k_cache, 
 /*
  * msa_workspace_bytes -- device scratch needed by an operation:
  *   MSA_OP_INVERT: n_rows query rows, n_req requests;
- *   MSA_OP_DECODE: n_rows = B decode requests (n_req ignored).
+ *   MSA_OP_DECODE: n_rows = B decode requests (n_req ignored);
+ *   MSA_OP_PREFILL: n_rows query rows, n_req requests.
  * Returns 0 for invalid arguments.
  */
 size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_dims_t *dims);

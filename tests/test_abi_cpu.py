@@ -90,7 +90,7 @@ def test_attention_shape_limits(lib):
     for kw in (dict(Hq=16, G=8), dict(D=96), dict(sm_scale=0.0)):
         d = good_dims(**kw)
         rc = lib.msa_sparse_attn_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 1, 100,
-                                         ctypes.byref(d), FAKE, FAKE, FAKE, None)
+                                         ctypes.byref(d), FAKE, FAKE, FAKE, ctypes.c_size_t(1 << 30), FAKE, None)
         assert rc in (1, 2), kw
 
 
@@ -105,6 +105,13 @@ def test_workspace_sizes_and_errors(lib):
     assert dec == (((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
                    + ((8 * 8 * 4 + 255) // 256) * 256)
     assert lib.msa_workspace_bytes(9, 8, 1, ctypes.byref(d)) == 0
+    # prefill work list: 16-byte header + one {key, first tile} pair per chunk of <= 8 tiles,
+    # at most one partial chunk per key plus the entries split into full chunks of 8 x 16 entries
+    pre = lib.msa_workspace_bytes(2, 8192, 1, ctypes.byref(d))
+    assert pre == 16 + 8 * (8 * 533 + (8192 * 8 * 16 + 127) // 128)
+    rc = lib.msa_sparse_attn_prefill(*([FAKE] * 8), 8192, 1, 4096, ctypes.byref(d), FAKE, FAKE, FAKE,
+                                     ctypes.c_size_t(pre - 1), FAKE, None)
+    assert rc == 6
     # too small a workspace is refused before any launch
     rc = lib.msa_invert_selection(FAKE, FAKE, 8192, 1, ctypes.byref(d), FAKE, FAKE, FAKE, ctypes.c_size_t(inv - 1),
                                   FAKE, None)
