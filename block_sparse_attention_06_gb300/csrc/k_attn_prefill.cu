@@ -15,12 +15,14 @@
 // from an atomic counter in key order, so a block selected by thousands of
 // queries is spread over many SMs while its K/V stays in L2.
 //
-// One CTA (10 warps):
-//   warp 0     producer: per chunk, K_j and V_j by TMA (128B swizzle, 64-column
-//              boxes) into one of two K/V buffers; per tile, decodes the entries
-//              (query row, slot, causal limit) into a ring of tile descriptors and
-//              gathers the HPG heads of each entry's query row by TMA into one of
-//              two Q buffers;
+// One CTA (11 warps):
+//   warp 0     decoder: takes chunks, loads K_j and V_j by TMA (128B swizzle,
+//              64-column boxes) into one of two K/V buffers, and decodes a whole
+//              chunk's entries (query row, slot, causal limit) at once, four per
+//              lane with the loads batched, into a ring of tile descriptors;
+//   warp 10    Q loader: per described tile, gathers the HPG heads of each
+//              entry's query row by TMA into one of two Q buffers as soon as the
+//              buffer is free, then hands the descriptor to the consumers;
 //   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
 //              K = D) into the S buffer of the tile's softmax group, then, once P
 //              is back in TMEM, O = P V with P as the TMEM A operand and V as an
@@ -38,9 +40,9 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kChunkTiles = 8;   // tiles per work chunk
-constexpr int kRing = 4;         // tile descriptors in flight
+constexpr int kRing = 16;        // tile descriptors in flight (two chunks)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -66,11 +68,19 @@ struct AttnSmem {
     uint64_t kv_full[2], kv_empty[2];
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-    uint64_t desc_full[kRing], desc_empty[kRing];
+    uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+
+// 2^x by the MUFU.EX2 hardware approximation (PTX ex2.approx.ftz.f32; relative
+// error about 2^-22, far below the bf16 rounding of P); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
 constexpr size_t kPlanHeaderBytes = 16;
@@ -172,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mbar_init(&sm.o_free[b], 4);
         }
         for (int r = 0; r < kRing; ++r) {
+            mbar_init(&sm.desc_ready[r], 32);
             mbar_init(&sm.desc_full[r], 32);
             mbar_init(&sm.desc_empty[r], 5);
         }
@@ -194,39 +205,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     const uint32_t tmem = sm.tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ decoder
+        constexpr int ENT_MAX = kChunkTiles * EPT;   // entries of a full chunk
+        constexpr int PER_LANE = ENT_MAX / 32;
         pdl_wait();   // the work list and the CSR come from the preceding kernels
         const int n_chunks = plan_hdr[1];
         const int per_g = n_req * max_blocks;
+        auto claim = [&]() {
+            int v = 0;
+            if (lane == 0) v = atomicAdd(plan_hdr, 1);
+            return __shfl_sync(0xffffffffu, v, 0);
+        };
         int u = 0;          // tiles described
-        int n_q = 0;        // tiles whose Q copies were issued
         int cs = 0;         // chunks whose K/V were loaded
         bool ok = true;
-        int c = 0;
-        if (lane == 0) c = atomicAdd(plan_hdr, 1);
-        c = __shfl_sync(0xffffffffu, c, 0);
+        int c = claim();
+        int2 ch = c < n_chunks ? chunks[c] : make_int2(0, 0);
         while (ok && c < n_chunks) {
-            int cn = 0;
-            if (lane == 0) cn = atomicAdd(plan_hdr, 1);
-            cn = __shfl_sync(0xffffffffu, cn, 0);
-            const int2 ch = chunks[c];
+            const int cn = claim();                                   // next chunk, header in flight
+            const int2 chn = cn < n_chunks ? chunks[cn] : make_int2(0, 0);
             const int key = ch.x, t0 = ch.y;
             const int g = key / per_g;
             const int req = (key - g * per_g) / max_blocks;
             const int j = key - g * per_g - req * max_blocks;
             const int off0 = blk_off[key], end0 = blk_off[key + 1];
             const int page = block_table[size_t(req) * max_blocks + j];
+            c = cn;
+            ch = chn;
             if (off0 < 0 || end0 > cap || off0 > end0 || page < 0 || page >= n_pages || g >= G) {
                 if (lane == 0) raise_flag(err, MSA_FLAG_BOUNDS);
-                c = cn;
                 continue;
             }
             const int off = off0 + t0 * EPT;
-            const int end = min(end0, off + kChunkTiles * EPT);
-            if (off >= end) {
-                c = cn;
-                continue;
-            }
+            const int end = min(end0, off + ENT_MAX);
+            if (off >= end) continue;
             const int nt = (end - off + EPT - 1) / EPT;
             const int kvb = cs & 1;
             if (cs >= 2) {
@@ -247,66 +259,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     tma_load_4d(sm.v[kvb] + i * 16384, &vmap, &sm.kv_full[kvb], i * 64, g, 0, page);
             }
             ++cs;
+            // decode the chunk's entries: all loads of a lane's PER_LANE entries are issued together
+            int ent[PER_LANE];
+#pragma unroll
+            for (int r = 0; r < PER_LANE; ++r) {
+                const int idx = off + lane + 32 * r;
+                ent[r] = idx < end ? blk_ent[idx] : -1;
+            }
+            int rq[PER_LANE], ps[PER_LANE];
+#pragma unroll
+            for (int r = 0; r < PER_LANE; ++r) {
+                const int v = ent[r] / topk;
+                const bool in = ent[r] >= 0 && v < n_rows;
+                rq[r] = in ? q_req[v] : -1;
+                ps[r] = in ? q_pos[v] : -1;
+            }
+            // the ring slots of this chunk's tiles must be free
             for (int t = 0; t < nt; ++t) {
-                const int slot = u % kRing, qb = u & 1;
-                if (u >= kRing) {
+                const int ut = u + t;
+                if (ut >= kRing) {
                     bool w = true;
-                    if (lane == 0) w = mbar_wait(&sm.desc_empty[slot], ((u / kRing) - 1) & 1, err, &sm.abort);
+                    if (lane == 0) w = mbar_wait(&sm.desc_empty[ut % kRing], ((ut / kRing) - 1) & 1, err, &sm.abort);
                     if (!__shfl_sync(0xffffffffu, w, 0)) {
                         ok = false;
                         break;
                     }
                 }
-                TileDesc &d = sm.desc[slot];
-                int qq = -1;
-                if (lane < EPT) {
-                    const int idx = off + t * EPT + lane;
-                    int sl = 0, lim = -1;
+            }
+            if (!ok) break;
+#pragma unroll
+            for (int r = 0; r < PER_LANE; ++r) {
+                const int i = lane + 32 * r;
+                if (i < nt * EPT) {
+                    const int idx = off + i;
+                    int qq = -1, sl = 0, lim = -1;
                     if (idx < end) {
-                        const int ent = blk_ent[idx];
-                        const int v = ent / topk;
-                        if (ent < 0 || v >= n_rows || q_req[v] != req) {
+                        const int v = ent[r] / topk;
+                        if (ent[r] < 0 || v >= n_rows || rq[r] != req) {
                             raise_flag(err, MSA_FLAG_BOUNDS);
                         } else {
-                            lim = q_pos[v] - j * 128;
+                            lim = ps[r] - j * 128;
                             if (lim < 0) {   // block past the row's position: not a candidate
                                 raise_flag(err, MSA_FLAG_BOUNDS);
                             } else {
                                 qq = v;
-                                sl = ent - v * topk;
+                                sl = ent[r] - v * topk;
                             }
                         }
                     }
-                    d.qq[lane] = qq;
-                    d.slot[lane] = sl;
-                    d.lim[lane] = lim;
+                    TileDesc &d = sm.desc[(u + i / EPT) % kRing];
+                    d.qq[i % EPT] = qq;
+                    d.slot[i % EPT] = sl;
+                    d.lim[i % EPT] = lim;
                 }
-                if (u >= 2) {
-                    bool w = true;
-                    if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((u >> 1) - 1) & 1, err, &sm.abort);
-                    if (!__shfl_sync(0xffffffffu, w, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (lane == 0) {
-                    d.flags = (kvb ? kFlagKv1 : 0) | (t == 0 ? kFlagFirst : 0) | (t == nt - 1 ? kFlagLast : 0);
-                    d.g = g;
-                    mbar_arrive_expect_tx(&sm.q_full[qb], 128 * D * 2);
-                }
-                __syncwarp();
-                if (lane < EPT) {
-                    const int row = qq >= 0 ? qq : n_rows;   // fully out of bounds -> zero rows
-#pragma unroll
-                    for (int i = 0; i < NSUB; ++i)
-                        tma_load_3d(sm.q[qb] + i * 16384 + lane * HPG * 128, &qmap, &sm.q_full[qb], i * 64,
-                                    g * HPG, row);
-                }
-                mbar_arrive(&sm.desc_full[slot]);
-                ++u;
-                n_q = u;
             }
-            c = cn;
+            if (lane < nt) {
+                TileDesc &d = sm.desc[(u + lane) % kRing];
+                d.flags = (kvb ? kFlagKv1 : 0) | (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
+                d.g = g;
+            }
+            for (int t = 0; t < nt; ++t) mbar_arrive(&sm.desc_ready[(u + t) % kRing]);
+            u += nt;
         }
         // two end markers, one for each softmax group (the MMA warp stops at the first)
         for (int e = 0; ok && e < 2; ++e) {
@@ -317,14 +330,49 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (!__shfl_sync(0xffffffffu, w, 0)) break;
             }
             if (lane == 0) sm.desc[slot].flags = kFlagEnd;
-            __syncwarp();
-            mbar_arrive(&sm.desc_full[slot]);
+            mbar_arrive(&sm.desc_ready[slot]);
             ++u;
         }
         if (sm.abort && lane == 0) {
-            // drain: the copies still in flight land before the CTA exits (u counts the two end
-            // markers only when the loop finished; tiles before them issued their Q copies)
+            // drain: the K/V copies still in flight land before the CTA exits
             for (int t = max(0, cs - 2); t < cs; ++t) mbar_wait(&sm.kv_full[t & 1], (t >> 1) & 1, err, nullptr);
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ Q loader
+        int n_q = 0;        // tiles whose Q copies were issued
+        int ends = 0;
+        for (int u = 0; ends < 2; ++u) {
+            const int slot = u % kRing;
+            // every lane waits (acquires) before it reads the descriptor
+            bool w = __all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort));
+            if (!w) break;
+            const volatile TileDesc &d = sm.desc[slot];
+            if (d.flags & kFlagEnd) {
+                ++ends;
+                mbar_arrive(&sm.desc_full[slot]);
+                continue;
+            }
+            const int qb = n_q & 1;
+            if (n_q >= 2) {
+                if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((n_q >> 1) - 1) & 1, err, &sm.abort);
+                if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            }
+            const int g = d.g;
+            const int qq = lane < EPT ? d.qq[lane] : -1;
+            if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qb], 128 * D * 2);
+            __syncwarp();
+            if (lane < EPT) {
+                const int row = qq >= 0 ? qq : n_rows;   // fully out of bounds -> zero rows
+#pragma unroll
+                for (int i = 0; i < NSUB; ++i)
+                    tma_load_3d(sm.q[qb] + i * 16384 + lane * HPG * 128, &qmap, &sm.q_full[qb], i * 64, g * HPG,
+                                row);
+            }
+            ++n_q;
+            mbar_arrive(&sm.desc_full[slot]);
+        }
+        if (sm.abort && lane == 0) {
+            // drain: the Q copies still in flight land before the CTA exits
             for (int t = max(0, n_q - 2); t < n_q; ++t) mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, err, nullptr);
         }
     } else if (warp == 1) {
@@ -386,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
-    } else {
+    } else if (warp >= 2 && warp < 10) {
         // ------------------------------------------------------------ softmax groups
         const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;                 // TMEM lanes this warp may access
@@ -411,42 +459,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
             float s[128];
+            {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(t_s + uint32_t(c0), v);
+                for (int c = 0; c < 4; ++c) tmem_ld32(t_s + uint32_t(c * 32), v[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(v[i]);
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
             }
-            float m = -INFINITY;
+            // row max as eight independent chains
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
             if (lim >= 127) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) m = fmaxf(m, s[c]);
+                for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
             } else {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     s[c] = c <= lim ? s[c] : -INFINITY;
-                    m = fmaxf(m, s[c]);
+                    mx[c & 7] = fmaxf(mx[c & 7], s[c]);
                 }
             }
+            const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float ms = m * scale;
-            // l: sum of the bf16-rounded probabilities the PV MMA consumes (normalises O);
-            // le: exact fp32 sum (gives the lse)
-            float l = 0.f, le = 0.f;
+            // probabilities 2^(s*scale - ms) as packed bf16 into TMEM; their fp32 sum in eight
+            // chains normalises O and gives the lse
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 64) {
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float pa = exp2f(fmaf(s[c0 + 2 * i], scale, -ms));
-                    const float pb = exp2f(fmaf(s[c0 + 2 * i + 1], scale, -ms));
+                    const float pa = fast_exp2(fmaf(s[c0 + 2 * i], scale, -ms));
+                    const float pb = fast_exp2(fmaf(s[c0 + 2 * i + 1], scale, -ms));
                     w[i] = pack_bf16x2(pa, pb);
-                    l += bf16_lo(w[i]) + bf16_hi(w[i]);
-                    le += pa + pb;
+                    acc[i & 7] += pa + pb;
                 }
                 tmem_st32(t_s + uint32_t(c0 >> 1), w);
             }
+            const float le = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -454,29 +511,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
-            uint32_t ov[D];
+            uint32_t ov[D / 32][32];
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(t_o + uint32_t(c0), v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) ov[c0 + i] = v[i];
-            }
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + uint32_t(c * 32), ov[c]);
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.o_free[wg]);
             if (qq >= 0) {
-                const float inv = 1.0f / l;
+                const float inv = 1.0f / le;
                 const size_t unit = (size_t(qq) * topk + sl) * size_t(Hq) + size_t(g) * HPG + h;
                 uint16_t *dst = o_part + unit * D;
 #pragma unroll
                 for (int i = 0; i < D; i += 8) {
+                    const uint32_t *o8 = &ov[i >> 5][i & 31];
                     uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ov[i + 0]) * inv, __uint_as_float(ov[i + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+                    w.x = pack_bf16x2(__uint_as_float(o8[0]) * inv, __uint_as_float(o8[1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(o8[2]) * inv, __uint_as_float(o8[3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(o8[4]) * inv, __uint_as_float(o8[5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(o8[6]) * inv, __uint_as_float(o8[7]) * inv);
                     *reinterpret_cast<uint4 *>(dst + i) = w;
                 }
                 lse_part[unit] = (ms + log2f(le)) * kLn2;
