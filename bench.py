@@ -327,7 +327,7 @@ def bench_prefill(args, world, dev, peaks, peak_src):
         msa.msa_sparse_attn_prefill(pc.q, pc.k_cache, pc.v_cache, pc.block_table, pc.q_req, pc.q_pos,
                                     ps.blk_off, ps.blk_ent, pd, ps.o_part, ps.lse_part, ps.attn_ws, err_word=ps.err)
         a_e[k].record()
-        msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, pd, ps.out, ps.lse, err_word=ps.err)
+        msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, ps.ent_pos, pd, ps.out, ps.lse, err_word=ps.err)
     p1.record()
     torch.cuda.synchronize()
     barrier(world)

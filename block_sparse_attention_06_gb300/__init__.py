@@ -69,9 +69,9 @@ def _load() -> ctypes.CDLL:
         "msa_index_score": [P, P, P, P, P, I, I, I, D, I, P, P, P],
         "msa_topk_blocks": [P, P, I, D, P, P, P],
         "msa_build_page_table": [P, P, P, I, I, D, P, P, P, P],
-        "msa_invert_selection": [P, P, I, I, D, P, P, P, S, P, P],
+        "msa_invert_selection": [P, P, I, I, D, P, P, P, P, S, P, P],
         "msa_sparse_attn_prefill": [P, P, P, P, P, P, P, P, I, I, I, D, P, P, P, S, P, P],
-        "msa_lse_merge": [P, P, P, I, D, P, P, P, P],
+        "msa_lse_merge": [P, P, P, P, I, D, P, P, P, P],
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
         "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
         "msa_check": [P, P],
@@ -200,8 +200,10 @@ def msa_build_page_table(sel, block_table, seq_lens, n_pages: int, dims: Dims, p
     return page_table, row_len
 
 
-def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_ent=None, workspace=None,
-                         err_word=None):
+def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_ent=None, ent_pos=None,
+                         workspace=None, err_word=None):
+    """-> (blk_off, blk_ent, ent_pos): the {block -> queries} CSR and each selected
+    (row, group, slot)'s position in it."""
     n_rows = sel.shape[0]
     _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
     _req(q_req, torch.int32, "q_req", (n_rows,))
@@ -215,6 +217,9 @@ def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_e
     _req(blk_ent, torch.int32, "blk_ent")
     if blk_ent.numel() < n_rows * dims.G * dims.topk:
         raise ValueError("blk_ent too small")
+    if ent_pos is None:
+        ent_pos = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, device=dev)
+    _req(ent_pos, torch.int32, "ent_pos", (n_rows, dims.G, dims.topk))
     need = msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
@@ -222,8 +227,8 @@ def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_e
     err_word = new_err_word(dev) if err_word is None else err_word
     d = dims.c()
     _call("msa_invert_selection", _ptr(sel), _ptr(q_req), n_rows, n_req, ctypes.byref(d), _ptr(blk_off),
-          _ptr(blk_ent), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
-    return blk_off, blk_ent
+          _ptr(blk_ent), _ptr(ent_pos), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
+    return blk_off, blk_ent, ent_pos
 
 
 def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, dims: Dims,
@@ -241,12 +246,13 @@ def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_
     _req(blk_off, torch.int32, "blk_off", (dims.G * n_req * dims.max_blocks + 1,))
     _req(blk_ent, torch.int32, "blk_ent")
     dev = q.device
+    n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
     if o_part is None:
-        o_part = torch.empty((n_rows, dims.topk, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
+        o_part = torch.empty((n_ent, hpg, dims.D), dtype=torch.bfloat16, device=dev)
     if lse_part is None:
-        lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, device=dev)
-    _req(o_part, torch.bfloat16, "o_part", (n_rows, dims.topk, dims.Hq, dims.D))
-    _req(lse_part, torch.float32, "lse_part", (n_rows, dims.topk, dims.Hq))
+        lse_part = torch.empty((n_ent, hpg), dtype=torch.float32, device=dev)
+    _req(o_part, torch.bfloat16, "o_part", (n_ent, hpg, dims.D))
+    _req(lse_part, torch.float32, "lse_part", (n_ent, hpg))
     need = msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
@@ -259,11 +265,13 @@ def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_
     return o_part, lse_part
 
 
-def msa_lse_merge(o_part, lse_part, sel, dims: Dims, out=None, lse=None, err_word=None):
-    n_rows = o_part.shape[0]
-    _req(o_part, torch.bfloat16, "o_part", (n_rows, dims.topk, dims.Hq, dims.D))
-    _req(lse_part, torch.float32, "lse_part", (n_rows, dims.topk, dims.Hq))
+def msa_lse_merge(o_part, lse_part, sel, ent_pos, dims: Dims, out=None, lse=None, err_word=None):
+    n_rows = sel.shape[0]
+    n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
+    _req(o_part, torch.bfloat16, "o_part", (n_ent, hpg, dims.D))
+    _req(lse_part, torch.float32, "lse_part", (n_ent, hpg))
     _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    _req(ent_pos, torch.int32, "ent_pos", (n_rows, dims.G, dims.topk))
     dev = o_part.device
     if out is None:
         out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
@@ -273,8 +281,8 @@ def msa_lse_merge(o_part, lse_part, sel, dims: Dims, out=None, lse=None, err_wor
     _req(lse, torch.float32, "lse", (n_rows, dims.Hq))
     err_word = new_err_word(dev) if err_word is None else err_word
     d = dims.c()
-    _call("msa_lse_merge", _ptr(o_part), _ptr(lse_part), _ptr(sel), n_rows, ctypes.byref(d), _ptr(out),
-          _ptr(lse), _ptr(err_word), _stream(dev))
+    _call("msa_lse_merge", _ptr(o_part), _ptr(lse_part), _ptr(sel), _ptr(ent_pos), n_rows, ctypes.byref(d),
+          _ptr(out), _ptr(lse), _ptr(err_word), _stream(dev))
     return out, lse
 
 
@@ -412,12 +420,14 @@ class PrefillStep:
         n_keys = dims.G * n_req * dims.max_blocks
         self.blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, **f)
         self.blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, **f)
+        self.ent_pos = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, **f)
         self.inv_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)),),
                                   dtype=torch.uint8, **f)
         self.attn_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)),),
                                    dtype=torch.uint8, **f)
-        self.o_part = torch.empty((n_rows, dims.topk, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
-        self.lse_part = torch.empty((n_rows, dims.topk, dims.Hq), dtype=torch.float32, **f)
+        n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
+        self.o_part = torch.empty((n_ent, hpg, dims.D), dtype=torch.bfloat16, **f)
+        self.lse_part = torch.empty((n_ent, hpg), dtype=torch.float32, **f)
         self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
         self.err = new_err_word(device)
@@ -427,13 +437,32 @@ class PrefillStep:
         msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
                         scores=self.scores, err_word=self.err)
         msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
-        msa_invert_selection(self.sel, q_req, self.n_req, self.dims, self.blk_off, self.blk_ent, self.inv_ws,
-                             err_word=self.err)
+        msa_invert_selection(self.sel, q_req, self.n_req, self.dims, self.blk_off, self.blk_ent, self.ent_pos,
+                             self.inv_ws, err_word=self.err)
 
     def attend(self, q, k_cache, v_cache, block_table, q_req, q_pos):
         msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, self.blk_off, self.blk_ent,
                                 self.dims, self.o_part, self.lse_part, self.attn_ws, err_word=self.err)
-        return msa_lse_merge(self.o_part, self.lse_part, self.sel, self.dims, self.out, self.lse, err_word=self.err)
+        return msa_lse_merge(self.o_part, self.lse_part, self.sel, self.ent_pos, self.dims, self.out, self.lse,
+                             err_word=self.err)
+
+    def partials_by_slot(self):
+        """The partials rearranged as [rows][topk][Hq][D] / [rows][topk][Hq] (host copies;
+        slots with sel < 0 hold zeros / -inf).  For inspection and tests."""
+        sel, pos = self.sel.cpu(), self.ent_pos.cpu()
+        n_rows, G, k = sel.shape
+        hpg = self.dims.Hq // G
+        op = self.o_part.cpu()
+        lp = self.lse_part.cpu()
+        valid = sel >= 0
+        p = torch.where(valid, pos, torch.zeros_like(pos)).long()
+        o = op[p]                                  # [rows][G][k][hpg][D]
+        lse = lp[p]                                # [rows][G][k][hpg]
+        o = torch.where(valid[..., None, None], o, torch.zeros_like(o))
+        lse = torch.where(valid[..., None], lse, torch.full_like(lse, float("-inf")))
+        o = o.permute(0, 2, 1, 3, 4).reshape(n_rows, k, G * hpg, -1)
+        lse = lse.permute(0, 2, 1, 3).reshape(n_rows, k, G * hpg)
+        return o, lse
 
     def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, q_req, q_pos):
         self.select(q_idx, kidx_cache, block_table, q_req, q_pos)

@@ -30,7 +30,8 @@
 //   warps 2-5, 6-9  two softmax groups that take alternate tiles: tcgen05.ld of
 //              S (thread = row), causal mask, exp2 softmax, P as packed bf16
 //              written over S (tcgen05.st), then tcgen05.ld of O, normalisation,
-//              bf16 partial and lse stores.  While one group runs its softmax
+//              bf16 partial and lse stores.  Partials are written in CSR-entry
+//              order: a tile's output rows are one contiguous block.  While one group runs its softmax
 //              the tensor core works on the other group's tile.
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D of 512 columns).
 // Every wait is bounded; a timeout raises MSA_FLAG_TIMEOUT and every role drains.
@@ -54,6 +55,7 @@ constexpr int kFlagEnd = 8;      // no more work
 struct TileDesc {
     int32_t flags;
     int32_t g;
+    int32_t ent0;      // CSR index of the tile's first entry (its output goes to partial rows ent0 ..)
     int32_t qq[32];    // query row of each entry, -1 for padding / rejected entries
     int32_t slot[32];  // selection slot of the entry
     int32_t lim[32];   // tokens t <= lim of the block are visible to the entry
@@ -168,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long cap = 1LL * n_rows * G * topk;
-    const int Hq = G * HPG;
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 TileDesc &d = sm.desc[(u + lane) % kRing];
                 d.flags = (kvb ? kFlagKv1 : 0) | (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
                 d.g = g;
+                d.ent0 = off + lane * EPT;
             }
             for (int t = 0; t < nt; ++t) mbar_arrive(&sm.desc_ready[(u + t) % kRing]);
             u += nt;
@@ -450,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort))) break;
             const volatile TileDesc &d = sm.desc[slot];
             if (d.flags & kFlagEnd) break;
-            const int g = d.g;
-            const int qq = d.qq[e], sl = d.slot[e];
+            const int qq = d.qq[e];
+            const int idx = d.ent0 + e;                  // CSR entry of this row
             const int lim = qq >= 0 ? d.lim[e] : 127;   // padding rows: any finite softmax, never stored
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.desc_empty[slot]);
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (lane == 0) mbar_arrive(&sm.o_free[wg]);
             if (qq >= 0) {
                 const float inv = 1.0f / le;
-                const size_t unit = (size_t(qq) * topk + sl) * size_t(Hq) + size_t(g) * HPG + h;
+                const size_t unit = size_t(idx) * HPG + h;
                 uint16_t *dst = o_part + unit * D;
 #pragma unroll
                 for (int i = 0; i < D; i += 8) {

@@ -420,7 +420,8 @@ __global__ void __launch_bounds__(1024) k_inv_scan(const int32_t *__restrict__ c
 
 __global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, size_t words, size_t n_keys,
                            const int32_t *__restrict__ off, const int32_t *__restrict__ sel, int n_req,
-                           int G, int topk, int max_blocks, int32_t *__restrict__ ent) {
+                           int G, int topk, int max_blocks, int32_t *__restrict__ ent,
+                           int32_t *__restrict__ ent_pos) {
     const size_t key = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (key >= n_keys) return;
@@ -447,6 +448,7 @@ __global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, size_t words, si
             int slot = 0;
             for (int s = 0; s < topk; ++s)
                 if (sq[s] == j) slot = s;
+            ent_pos[(size_t(q) * G + g) * topk + slot] = pos;
             ent[pos++] = q * topk + slot;
         }
         base += __shfl_sync(0xffffffffu, x, 31);
@@ -515,7 +517,7 @@ size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s) {
 }
 
 cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
-                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, void *ws,
+                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws,
                           int32_t *err, cudaStream_t st) {
     const InvLayout l = inv_layout(n_rows, n_req, s.G, s.max_blocks);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -532,7 +534,7 @@ cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, 
     k_inv_count<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, cnt);
     k_inv_scan<<<1, 1024, 0, st>>>(cnt, l.n_keys, blk_off);
     k_inv_emit<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, blk_off, sel, n_req, s.G, s.topk,
-                                      s.max_blocks, blk_ent);
+                                      s.max_blocks, blk_ent, ent_pos);
     return cudaGetLastError();
 }
 

@@ -185,8 +185,9 @@ msa_status_t msa_build_page_table(const int32_t *sel, const int32_t *block_table
 }
 
 msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int32_t n_rows, int32_t n_req,
-                                  const msa_dims_t *dims, int32_t *blk_off, int32_t *blk_ent, void *workspace,
-                                  size_t workspace_bytes, int32_t *err_word, msa_stream_t stream) {
+                                  const msa_dims_t *dims, int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                  msa_stream_t stream) {
     Shape s;
     msa_status_t st = check_dims(dims, false, false, &s, "msa_invert_selection");
     if (st != MSA_OK) return st;
@@ -195,12 +196,13 @@ msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int3
     MSA_REQUIRE(q_req || n_rows == 0, "msa_invert_selection: NULL q_req");
     MSA_REQUIRE(blk_off && err_word, "msa_invert_selection: NULL pointer");
     MSA_REQUIRE(blk_ent || n_rows == 0, "msa_invert_selection: NULL blk_ent");
+    MSA_REQUIRE(ent_pos || n_rows == 0, "msa_invert_selection: NULL ent_pos");
     if (1.0 * n_rows * s.G * s.topk > 2147483647.0)
         return fail(MSA_ERR_UNSUPPORTED, "msa_invert_selection: more than 2^31 entries");
     const size_t need = invert_workspace_bytes(n_rows, n_req, s);
     if (!workspace || workspace_bytes < need)
         return fail(MSA_ERR_WORKSPACE, "msa_invert_selection: workspace needs %zu bytes", need);
-    cudaError_t e = launch_invert(sel, q_req, n_rows, n_req, s, blk_off, blk_ent, workspace, err_word,
+    cudaError_t e = launch_invert(sel, q_req, n_rows, n_req, s, blk_off, blk_ent, ent_pos, workspace, err_word,
                                   static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_invert_selection");
 }
@@ -232,16 +234,19 @@ msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const v
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_attn_prefill");
 }
 
-msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel, int32_t n_rows,
-                           const msa_dims_t *dims, void *out, float *lse, int32_t *err_word, msa_stream_t stream) {
+msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel, const int32_t *ent_pos,
+                           int32_t n_rows, const msa_dims_t *dims, void *out, float *lse, int32_t *err_word,
+                           msa_stream_t stream) {
     Shape s;
     msa_status_t st = check_dims(dims, false, false, &s, "msa_lse_merge");
     if (st != MSA_OK) return st;
     if (s.D != 64 && s.D != 128) return fail(MSA_ERR_UNSUPPORTED, "msa_lse_merge: D must be 64 or 128");
     MSA_REQUIRE(n_rows >= 0, "msa_lse_merge: n_rows < 0");
     if (n_rows == 0) return MSA_OK;
-    MSA_REQUIRE(o_part && lse_part && sel && out && lse && err_word, "msa_lse_merge: NULL pointer");
-    cudaError_t e = launch_lse_merge(o_part, lse_part, sel, n_rows, s, out, lse, err_word,
+    MSA_REQUIRE(o_part && lse_part && sel && ent_pos && out && lse && err_word, "msa_lse_merge: NULL pointer");
+    if (1.0 * n_rows * s.G * s.topk > 2147483647.0)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_lse_merge: more than 2^31 entries");
+    cudaError_t e = launch_lse_merge(o_part, lse_part, sel, ent_pos, n_rows, s, out, lse, err_word,
                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_lse_merge");
 }
@@ -351,6 +356,6 @@ const char *msa_status_str(msa_status_t status) {
 
 const char *msa_last_error(void) { return g_last_error; }
 
-int32_t msa_version(void) { return 200; }
+int32_t msa_version(void) { return 300; }
 
 }  // extern "C"

@@ -54,7 +54,7 @@ cudaError_t launch_page_table(const int32_t *sel, const int32_t *block_table, co
 
 size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s);
 cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
-                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, void *ws,
+                          const Shape &s, int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws,
                           int32_t *err, cudaStream_t st);
 
 // Block-major prefill attention: a plan kernel writes the chunk work list into
@@ -68,8 +68,8 @@ cudaError_t launch_attn_prefill(const void *q, const void *k_cache, const void *
                                 int32_t *err, cudaStream_t st);
 
 cudaError_t launch_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel,
-                             int n_rows, const Shape &s, void *out, float *lse, int32_t *err,
-                             cudaStream_t st);
+                             const int32_t *ent_pos, int n_rows, const Shape &s, void *out, float *lse,
+                             int32_t *err, cudaStream_t st);
 
 // Decode workspace: split-by-page partials, their lse, and one merge counter per
 // (request, group) row.  The counters must be zero when the attention kernel

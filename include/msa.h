@@ -152,35 +152,41 @@ msa_status_t msa_build_page_table(const int32_t *sel, const int32_t *block_table
  * the mapping is reorganised so attention can loop over KV blocks outside and
  * queries inside.  Keys are key = (g * n_req + q_req[q]) * max_blocks + block;
  * the output is a CSR whose entries are q * topk + slot, ascending in q inside
- * each key (deterministic, a stable counting sort).
+ * each key (deterministic, a stable counting sort).  ent_pos is the inverse
+ * map: the CSR position of each selected (row, group, slot), which is also the
+ * row of that slot's partial in msa_sparse_attn_prefill's output.
  *
  *   sel      int32 [n_rows][G][topk]
  *   q_req    int32 [n_rows]
  *   blk_off  int32 [G * n_req * max_blocks + 1]  out
  *   blk_ent  int32 [n_rows * G * topk]           out (first blk_off[last] used)
+ *   ent_pos  int32 [n_rows][G][topk]             out; blk_ent[ent_pos[q][g][s]] ==
+ *                                                q * topk + s where sel[q][g][s] >= 0,
+ *                                                unwritten where sel < 0
  *   workspace device scratch of msa_workspace_bytes(MSA_OP_INVERT, ...) bytes
  */
 msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int32_t n_rows,
                                   int32_t n_req, const msa_dims_t *dims, int32_t *blk_off,
-                                  int32_t *blk_ent, void *workspace, size_t workspace_bytes,
-                                  int32_t *err_word, msa_stream_t stream);
+                                  int32_t *blk_ent, int32_t *ent_pos, void *workspace,
+                                  size_t workspace_bytes, int32_t *err_word, msa_stream_t stream);
 
 /*
  * msa_sparse_attn_prefill -- KV-block-major sparse attention.  [T-zh KV 块主序稀疏注意力]
  * and [T-ja, KV block-major kernel paragraph]: for each (group, KV block) the
  * block's K and V are read once and every query that selected it attends it;
  * [NV-ja]: each KV cache block is read once with contiguous access.  For each
- * CSR entry (q, slot) of key (g, req, j) and each head h of group g, writes the
- * softmax-normalised partial output over block j's tokens at positions <=
- * q_pos[q], and its log-sum-exp (natural log of the sum of exp of the
- * sm_scale-scaled logits).  Slots without an entry are not written.
+ * CSR entry i = (q, slot) of key (g, req, j) and each head hh < Hq/G of group
+ * g, writes the softmax-normalised partial output over block j's tokens at
+ * positions <= q_pos[q], and its log-sum-exp (natural log of the sum of exp of
+ * the sm_scale-scaled logits), at partial row i (CSR order, so the rows a tile
+ * of one key produces are contiguous).  Rows past blk_off[last] are not written.
  *
  *   q        bf16 [n_rows][Hq][D]
  *   k_cache, v_cache bf16 [n_pages][128][G][D]
  *   block_table int32 [n_req][max_blocks];  q_req, q_pos int32 [n_rows]
  *   blk_off, blk_ent  the CSR of msa_invert_selection (same n_req, dims)
- *   o_part   bf16 [n_rows][topk][Hq][D]  out
- *   lse_part fp32 [n_rows][topk][Hq]     out
+ *   o_part   bf16 [n_rows * G * topk][Hq/G][D]  out (entry-major)
+ *   lse_part fp32 [n_rows * G * topk][Hq/G]     out
  *   workspace device scratch of msa_workspace_bytes(MSA_OP_PREFILL, n_rows,
  *            n_req, ...) bytes, 16-byte aligned: the work list (each key cut
  *            into chunks of at most 8 tiles of 128/(Hq/G) entries) that one
@@ -197,18 +203,21 @@ msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const v
 /*
  * msa_lse_merge -- Log-Sum-Exp reduction of per-block partials.  [T-zh KV
  * 块主序稀疏注意力]: the partial O of each KV block is rescaled and summed.  For
- * each (q, h) over the slots s with sel[q][h / (Hq/G)][s] >= 0:
+ * each (q, h), g = h / (Hq/G), hh = h % (Hq/G), over the slots s with
+ * sel[q][g][s] >= 0, the partial O_s / lse_s being row ent_pos[q][g][s], head hh
+ * of o_part / lse_part:
  *   lse = m + log(sum_s exp(lse_s - m)),  m = max_s lse_s
  *   out = sum_s exp(lse_s - lse) * O_s
- * Slots with sel < 0 are never read.
+ * Slots with sel < 0 are never read.  An ent_pos outside [0, n_rows*G*topk)
+ * raises MSA_FLAG_BOUNDS and that slot is skipped.
  *
- *   o_part   bf16 [n_rows][topk][Hq][D];  lse_part fp32 [n_rows][topk][Hq]
- *   sel      int32 [n_rows][G][topk]
+ *   o_part   bf16 [n_rows * G * topk][Hq/G][D];  lse_part fp32 [n_rows * G * topk][Hq/G]
+ *   sel, ent_pos  int32 [n_rows][G][topk]
  *   out      bf16 [n_rows][Hq][D]  out;  lse fp32 [n_rows][Hq]  out
  */
 msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int32_t *sel,
-                           int32_t n_rows, const msa_dims_t *dims, void *out, float *lse,
-                           int32_t *err_word, msa_stream_t stream);
+                           const int32_t *ent_pos, int32_t n_rows, const msa_dims_t *dims, void *out,
+                           float *lse, int32_t *err_word, msa_stream_t stream);
 
 /*
  * msa_sparse_attn_decode -- decode attention over per-(request, group) page

@@ -78,6 +78,22 @@ def assert_lse(gpu_lse, ref_lse, what="lse"):
     assert float(d.max()) <= LSE_ATOL, f"{what}: max abs err {float(d.max()):.3e} > {LSE_ATOL}"
 
 
+def assert_ent_pos(sel, ent_pos, ent):
+    """ent_pos is the inverse of the CSR entry list: the entry at position
+    ent_pos[q][g][s] is (q, slot s) for every selected (q, g, s), and every CSR
+    position is claimed once."""
+    sel, pos = sel.cpu(), ent_pos.cpu()
+    n_rows, G, k = sel.shape
+    valid = sel >= 0
+    p = pos[valid].long()
+    assert int(p.numel()) == int(ent.numel())
+    assert bool((p >= 0).all()) and bool((p < ent.numel()).all())
+    q = torch.arange(n_rows)[:, None, None].expand(n_rows, G, k)[valid]
+    s = torch.arange(k)[None, None, :].expand(n_rows, G, k)[valid]
+    assert torch.equal(ent[p].long(), (q * k + s).long())
+    assert int(torch.unique(p).numel()) == int(p.numel())
+
+
 def compact_pages(block_table: torch.Tensor, sel: torch.Tensor, q_req: torch.Tensor):
     """Pages a selection touches, and a block table remapped onto a compact pool
     holding only those pages (unselected blocks map to page 0)."""

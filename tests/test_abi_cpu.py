@@ -78,7 +78,8 @@ def test_null_pointers_and_bad_sizes(lib):
     assert lib.msa_topk_blocks(FAKE, None, 4, ctypes.byref(d), FAKE, FAKE, None) == 1
     assert lib.msa_topk_blocks(FAKE, FAKE, -1, ctypes.byref(d), FAKE, FAKE, None) == 1
     assert lib.msa_build_page_table(FAKE, FAKE, FAKE, 2, 0, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
-    assert lib.msa_lse_merge(FAKE, FAKE, None, 4, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
+    assert lib.msa_lse_merge(FAKE, FAKE, None, FAKE, 4, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
+    assert lib.msa_lse_merge(FAKE, FAKE, FAKE, None, 4, ctypes.byref(d), FAKE, FAKE, FAKE, None) == 1
     assert lib.msa_check(None, None) == 1
     # empty work is a no-op that never touches the device
     assert lib.msa_topk_blocks(None, None, 0, ctypes.byref(d), None, None, None) == 0
@@ -113,7 +114,7 @@ def test_workspace_sizes_and_errors(lib):
                                      ctypes.c_size_t(pre - 1), FAKE, None)
     assert rc == 6
     # too small a workspace is refused before any launch
-    rc = lib.msa_invert_selection(FAKE, FAKE, 8192, 1, ctypes.byref(d), FAKE, FAKE, FAKE, ctypes.c_size_t(inv - 1),
+    rc = lib.msa_invert_selection(FAKE, FAKE, 8192, 1, ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, ctypes.c_size_t(inv - 1),
                                   FAKE, None)
     assert rc == 6
     rc = lib.msa_sparse_attn_decode(FAKE, FAKE, FAKE, FAKE, FAKE, 8, 4096, ctypes.byref(good_dims()), FAKE, FAKE,

@@ -43,18 +43,20 @@ def _check_prefill(m, case, rows=None, check_partials=True):
     gap = P.selection_gap(ref_sc, q_pos, case.dims.topk)
     gsel = step.sel.cpu()[idx]
     P.assert_selection_where_unambiguous(gsel, ref_sel, gap)
-    # inversion of the GPU's full selection is bit-exact
+    # inversion of the GPU's full selection is bit-exact, and ent_pos is its inverse
     off, ent = oracle.invert(step.sel.cpu(), case.q_req.cpu(), case.n_req, case.max_blocks)
     assert torch.equal(step.blk_off.cpu(), off)
     assert torch.equal(step.blk_ent.cpu()[:int(off[-1])], ent)
+    P.assert_ent_pos(step.sel.cpu(), step.ent_pos.cpu(), ent)
     # per-block partials (valid slots) and the merged output on the GPU's selection
     if check_partials:
         kc, vc = case.k_cache.cpu(), case.v_cache.cpu()
         op, lp = oracle.block_partials(case.q.cpu()[idx], kc, vc, local_bt, local, q_pos, gsel, case.dims.sm_scale)
         hpg = case.dims.Hq // case.dims.G
         valid = (gsel >= 0).repeat_interleave(hpg, dim=1).transpose(1, 2)   # [rows][topk][Hq]
-        P.assert_lse(step.lse_part.cpu()[idx][valid], lp[valid], "lse_part")
-        P.assert_out(step.o_part.cpu()[idx][valid], op[valid], "o_part")
+        o_by_slot, l_by_slot = step.partials_by_slot()
+        P.assert_lse(l_by_slot[idx][valid], lp[valid], "lse_part")
+        P.assert_out(o_by_slot[idx][valid], op[valid], "o_part")
     o_ref, l_ref = P.oracle_attention_on(case, rows, gsel)
     P.assert_out(step.out.cpu()[idx], o_ref)
     P.assert_lse(step.lse.cpu()[idx], l_ref)
@@ -124,20 +126,32 @@ def test_invert_bit_exact_multi_request(msa):
             c = int(torch.randint(1, k + 1, (1,), generator=gen))
             sel[q, g, :c] = torch.randperm(mb, generator=gen)[:c].sort().values.to(torch.int32)
     dims = msa.Dims(16, G, 128, 64, k, mb)
-    off, ent = msa.msa_invert_selection(sel.to(DEV), q_req.to(DEV), n_req, dims)
+    off, ent, pos = msa.msa_invert_selection(sel.to(DEV), q_req.to(DEV), n_req, dims)
     roff, rent = oracle.invert(sel, q_req, n_req, mb)
     assert torch.equal(off.cpu(), roff)
     assert torch.equal(ent.cpu()[:int(roff[-1])], rent)
+    P.assert_ent_pos(sel, pos.cpu(), rent)
 
 
 def test_lse_merge_matches_oracle(msa):
+    """The merge on partials stored in an arbitrary entry order (ent_pos a random
+    permutation), against the oracle's merge of the same partials by slot."""
     gen = torch.Generator().manual_seed(2)
     n_rows, G, Hq, D, k = 64, 4, 32, 128, 9
+    hpg = Hq // G
     sel = torch.randint(-1, 20, (n_rows, G, k), generator=gen, dtype=torch.int32)
     o = torch.randn(n_rows, k, Hq, D, generator=gen).to(torch.bfloat16)
     lse = torch.randn(n_rows, k, Hq, generator=gen) * 3
+    n_ent = n_rows * G * k
+    ent_pos = torch.randperm(n_ent, generator=gen).to(torch.int32).reshape(n_rows, G, k)
+    o_ent = torch.zeros(n_ent, hpg, D, dtype=torch.bfloat16)
+    l_ent = torch.zeros(n_ent, hpg)
+    o_g = o.reshape(n_rows, k, G, hpg, D).permute(0, 2, 1, 3, 4)      # [rows][G][k][hpg][D]
+    l_g = lse.reshape(n_rows, k, G, hpg).permute(0, 2, 1, 3)
+    o_ent[ent_pos.long().flatten()] = o_g.reshape(-1, hpg, D)
+    l_ent[ent_pos.long().flatten()] = l_g.reshape(-1, hpg)
     dims = msa.Dims(Hq, G, D, 64, k, 20)
-    out, l = msa.msa_lse_merge(o.to(DEV), lse.to(DEV), sel.to(DEV), dims)
+    out, l = msa.msa_lse_merge(o_ent.to(DEV), l_ent.to(DEV), sel.to(DEV), ent_pos.to(DEV), dims)
     valid = (sel >= 0).repeat_interleave(Hq // G, dim=1).transpose(1, 2)
     lse_m = torch.where(valid, lse.double(), torch.tensor(float("-inf"), dtype=torch.float64))
     ro, rl = oracle.lse_merge(o.double() * valid[..., None], lse_m)
