@@ -13,26 +13,31 @@
 // dimension.  A plan kernel cuts every key into chunks of at most kChunkTiles
 // tiles; the attention kernel runs one persistent CTA per SM that takes chunks
 // from an atomic counter in key order, so a block selected by thousands of
-// queries is spread over many SMs while its K/V stays in L2.
+// queries is spread over many SMs while its K/V stays in L2.  Partials are
+// written in CSR-entry order, so the output of one tile is one contiguous block.
 //
-// One CTA (11 warps):
-//   warp 0     decoder: takes chunks, loads K_j and V_j by TMA (128B swizzle,
-//              64-column boxes) into one of two K/V buffers, and decodes a whole
-//              chunk's entries (query row, slot, causal limit) at once, four per
-//              lane with the loads batched, into a ring of tile descriptors;
-//   warp 10    Q loader: per described tile, gathers the HPG heads of each
-//              entry's query row by TMA into one of two Q buffers as soon as the
-//              buffer is free, then hands the descriptor to the consumers;
+// One CTA (12 warps):
+//   warp 0     decoder: takes chunks, loads K_j by TMA (128B swizzle, 64-column
+//              boxes) into one of two K buffers, warms L2 with V_j and hands the
+//              chunk to the V loader, and decodes a whole chunk's entries (query
+//              row, slot, causal limit) at once, with the loads batched, into a
+//              ring of tile descriptors;
+//   warp 3     lane 0, V loader: V_j by TMA into the V buffer once the previous
+//              chunk's last PV has completed; lane 1, output store: the staged
+//              tile goes to the partials by TMA bulk tensor stores in a few
+//              power-of-two row boxes, then the staging buffer is handed on;
+//   warp 2     Q loader: gathers the HPG heads of each entry's query row by TMA
+//              into one of two Q buffers;
 //   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
 //              K = D) into the S buffer of the tile's softmax group, then, once P
 //              is back in TMEM, O = P V with P as the TMEM A operand and V as an
 //              MN-major shared-memory B operand;
-//   warps 2-5, 6-9  two softmax groups that take alternate tiles: tcgen05.ld of
-//              S (thread = row), causal mask, exp2 softmax, P as packed bf16
-//              written over S (tcgen05.st), then tcgen05.ld of O, normalisation,
-//              bf16 partial and lse stores.  Partials are written in CSR-entry
-//              order: a tile's output rows are one contiguous block.  While one group runs its softmax
-//              the tensor core works on the other group's tile.
+//   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
+//              from TMEM in 32-column chunks twice (row max, then exp2 and P as
+//              packed bf16 written over S), then O chunk by chunk, normalised,
+//              into the shared staging buffer in the 128B-swizzled box layout;
+//              while one group runs its softmax the tensor core works on the
+//              other group's tile.
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D of 512 columns).
 // Every wait is bounded; a timeout raises MSA_FLAG_TIMEOUT and every role drains.
 #include "msa_device.cuh"
@@ -41,13 +46,14 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kChunkTiles = 8;   // tiles per work chunk
 constexpr int kRing = 16;        // tile descriptors in flight (two chunks)
+constexpr int kStoreBoxes = 6;   // store boxes of 128, 64, 32, 16, 8, 4 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kFlagKv1 = 1;      // K/V buffer 1 (else 0)
+constexpr int kFlagKv1 = 1;      // K buffer 1 (else 0)
 constexpr int kFlagFirst = 2;    // first tile of its chunk
 constexpr int kFlagLast = 4;     // last tile of its chunk
 constexpr int kFlagEnd = 8;      // no more work
@@ -56,6 +62,7 @@ struct TileDesc {
     int32_t flags;
     int32_t g;
     int32_t ent0;      // CSR index of the tile's first entry (its output goes to partial rows ent0 ..)
+    int32_t n_valid;   // entries of this tile that exist (the rest is padding)
     int32_t qq[32];    // query row of each entry, -1 for padding / rejected entries
     int32_t slot[32];  // selection slot of the entry
     int32_t lim[32];   // tokens t <= lim of the block are visible to the entry
@@ -64,13 +71,17 @@ struct TileDesc {
 template <int D>
 struct AttnSmem {
     alignas(1024) uint8_t k[2][D * 128 * 2];
-    alignas(1024) uint8_t v[2][D * 128 * 2];
+    alignas(1024) uint8_t v[D * 128 * 2];
     alignas(1024) uint8_t q[2][128 * D * 2];
+    alignas(1024) uint8_t stg[128 * D * 2];         // one tile's bf16 output on its way to the partials
     TileDesc desc[kRing];
-    uint64_t kv_full[2], kv_empty[2];
+    int32_t chunk_page[4], chunk_g[4];              // decoder -> V loader
+    uint64_t k_full[2], k_empty[2], v_full, v_empty;
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t stg_full, stg_free;
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
+    uint64_t chunk_ready[4], chunk_free[4];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -152,14 +163,18 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const int32_t *__restrict__ 
 
 // ------------------------------------------------------------------ attention
 
+struct StoreMaps {
+    CUtensorMap box[kStoreBoxes];   // partials as [rows][D], boxes of 64 columns x (128 >> i) rows
+};
+
 template <int D, int HPG>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const int32_t *__restrict__ block_table,
-    const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos, const int32_t *__restrict__ blk_off,
-    const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr, const int2 *__restrict__ chunks,
-    int n_rows, int n_req, int n_pages, int G, int topk, int max_blocks, float sm_scale,
-    uint16_t *__restrict__ o_part, float *__restrict__ lse_part, int32_t *err) {
+    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ StoreMaps omaps,
+    const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos,
+    const int32_t *__restrict__ blk_off, const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr,
+    const int2 *__restrict__ chunks, int n_rows, int n_req, int n_pages, int G, int topk, int max_blocks,
+    float sm_scale, float *__restrict__ lse_part, int32_t *err) {
     constexpr int EPT = 128 / HPG;                 // entries per tile
     constexpr int NSUB = D / 64;                   // 64-column sub-tiles
     constexpr uint32_t kIdescS = make_idesc_bf16(128, 128, 0, 0);
@@ -173,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.kv_full[b], 1);
-            mbar_init(&sm.kv_empty[b], 1);
+            mbar_init(&sm.k_full[b], 1);
+            mbar_init(&sm.k_empty[b], 1);
             mbar_init(&sm.q_full[b], 1);
             mbar_init(&sm.q_empty[b], 1);
             mbar_init(&sm.s_full[b], 1);
@@ -182,10 +197,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mbar_init(&sm.o_full[b], 1);
             mbar_init(&sm.o_free[b], 4);
         }
+        mbar_init(&sm.v_full, 1);
+        mbar_init(&sm.v_empty, 1);
+        mbar_init(&sm.stg_full, 4);
+        mbar_init(&sm.stg_free, 1);
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.desc_ready[r], 32);
             mbar_init(&sm.desc_full[r], 32);
-            mbar_init(&sm.desc_empty[r], 5);
+            mbar_init(&sm.desc_empty[r], 6);
+        }
+        for (int r = 0; r < 4; ++r) {
+            mbar_init(&sm.chunk_ready[r], 1);
+            mbar_init(&sm.chunk_free[r], 1);
         }
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
@@ -199,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
+        for (int i = 0; i < kStoreBoxes; ++i) tma_prefetch_desc(&omaps.box[i]);
     }
     tc_fence_before();
     __syncthreads();
@@ -217,8 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (lane == 0) v = atomicAdd(plan_hdr, 1);
             return __shfl_sync(0xffffffffu, v, 0);
         };
+        auto wait_lane0 = [&](uint64_t *bar, uint32_t parity) -> bool {
+            bool w = true;
+            if (lane == 0) w = mbar_wait(bar, parity, err, &sm.abort);
+            return __shfl_sync(0xffffffffu, w, 0);
+        };
         int u = 0;          // tiles described
-        int cs = 0;         // chunks whose K/V were loaded
+        int cs = 0;         // chunks issued
         bool ok = true;
         int c = claim();
         int2 ch = c < n_chunks ? chunks[c] : make_int2(0, 0);
@@ -241,23 +270,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const int end = min(end0, off + ENT_MAX);
             if (off >= end) continue;
             const int nt = (end - off + EPT - 1) / EPT;
-            const int kvb = cs & 1;
-            if (cs >= 2) {
-                bool w = true;
-                if (lane == 0) w = mbar_wait(&sm.kv_empty[kvb], ((cs >> 1) - 1) & 1, err, &sm.abort);
-                if (!__shfl_sync(0xffffffffu, w, 0)) {
-                    ok = false;
-                    break;
-                }
+            const int kb = cs & 1;
+            // K into buffer kb once the last S of chunk cs-2 has completed; V warms L2 for the V loader
+            if (cs >= 2 && !wait_lane0(&sm.k_empty[kb], ((cs >> 1) - 1) & 1)) {
+                ok = false;
+                break;
             }
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.kv_full[kvb], 2 * D * 128 * 2);
+                mbar_arrive_expect_tx(&sm.k_full[kb], D * 128 * 2);
 #pragma unroll
-                for (int i = 0; i < NSUB; ++i)
-                    tma_load_4d(sm.k[kvb] + i * 16384, &kmap, &sm.kv_full[kvb], i * 64, g, 0, page);
-#pragma unroll
-                for (int i = 0; i < NSUB; ++i)
-                    tma_load_4d(sm.v[kvb] + i * 16384, &vmap, &sm.kv_full[kvb], i * 64, g, 0, page);
+                for (int i = 0; i < NSUB; ++i) {
+                    tma_load_4d(sm.k[kb] + i * 16384, &kmap, &sm.k_full[kb], i * 64, g, 0, page);
+                    tma_prefetch_l2_4d(&vmap, i * 64, g, 0, page);
+                }
+            }
+            if (cs >= 4 && !wait_lane0(&sm.chunk_free[cs & 3], ((cs >> 2) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                sm.chunk_page[cs & 3] = page;
+                sm.chunk_g[cs & 3] = g;
+                mbar_arrive(&sm.chunk_ready[cs & 3]);
             }
             ++cs;
             // decode the chunk's entries: all loads of a lane's PER_LANE entries are issued together
@@ -276,16 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 ps[r] = in ? q_pos[v] : -1;
             }
             // the ring slots of this chunk's tiles must be free
-            for (int t = 0; t < nt; ++t) {
+            for (int t = 0; ok && t < nt; ++t) {
                 const int ut = u + t;
-                if (ut >= kRing) {
-                    bool w = true;
-                    if (lane == 0) w = mbar_wait(&sm.desc_empty[ut % kRing], ((ut / kRing) - 1) & 1, err, &sm.abort);
-                    if (!__shfl_sync(0xffffffffu, w, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
+                if (ut >= kRing && !wait_lane0(&sm.desc_empty[ut % kRing], ((ut / kRing) - 1) & 1)) ok = false;
             }
             if (!ok) break;
 #pragma unroll
@@ -316,38 +343,87 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             }
             if (lane < nt) {
                 TileDesc &d = sm.desc[(u + lane) % kRing];
-                d.flags = (kvb ? kFlagKv1 : 0) | (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
+                d.flags = (kb ? kFlagKv1 : 0) | (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
                 d.g = g;
                 d.ent0 = off + lane * EPT;
+                d.n_valid = min(EPT, end - (off + lane * EPT));
             }
             for (int t = 0; t < nt; ++t) mbar_arrive(&sm.desc_ready[(u + t) % kRing]);
             u += nt;
         }
-        // two end markers, one for each softmax group (the MMA warp stops at the first)
+        // end markers: two tiles (one per softmax group; the MMA and store warps stop at the first), one chunk
         for (int e = 0; ok && e < 2; ++e) {
             const int slot = u % kRing;
-            if (u >= kRing) {
-                bool w = true;
-                if (lane == 0) w = mbar_wait(&sm.desc_empty[slot], ((u / kRing) - 1) & 1, err, &sm.abort);
-                if (!__shfl_sync(0xffffffffu, w, 0)) break;
-            }
+            if (u >= kRing && !wait_lane0(&sm.desc_empty[slot], ((u / kRing) - 1) & 1)) break;
             if (lane == 0) sm.desc[slot].flags = kFlagEnd;
             mbar_arrive(&sm.desc_ready[slot]);
             ++u;
         }
-        if (sm.abort && lane == 0) {
-            // drain: the K/V copies still in flight land before the CTA exits
-            for (int t = max(0, cs - 2); t < cs; ++t) mbar_wait(&sm.kv_full[t & 1], (t >> 1) & 1, err, nullptr);
+        if (ok && (cs < 4 || wait_lane0(&sm.chunk_free[cs & 3], ((cs >> 2) - 1) & 1))) {
+            if (lane == 0) {
+                sm.chunk_page[cs & 3] = -1;
+                mbar_arrive(&sm.chunk_ready[cs & 3]);
+            }
         }
-    } else if (warp == 10) {
+        if (sm.abort && lane == 0) {
+            // drain: the K copies still in flight land before the CTA exits
+            for (int t = max(0, cs - 2); t < cs; ++t) mbar_wait(&sm.k_full[t & 1], (t >> 1) & 1, err, nullptr);
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ V loader (lane 0)
+        if (lane == 0) {
+            int issued = 0;
+            for (int cs = 0;; ++cs) {
+                if (!mbar_wait(&sm.chunk_ready[cs & 3], (cs >> 2) & 1, err, &sm.abort)) break;
+                const int page = *reinterpret_cast<volatile int32_t *>(&sm.chunk_page[cs & 3]);
+                const int g = *reinterpret_cast<volatile int32_t *>(&sm.chunk_g[cs & 3]);
+                mbar_arrive(&sm.chunk_free[cs & 3]);
+                if (page < 0) break;
+                if (cs >= 1 && !mbar_wait(&sm.v_empty, (cs - 1) & 1, err, &sm.abort)) break;
+                mbar_arrive_expect_tx(&sm.v_full, D * 128 * 2);
+#pragma unroll
+                for (int i = 0; i < NSUB; ++i) tma_load_4d(sm.v + i * 16384, &vmap, &sm.v_full, i * 64, g, 0, page);
+                issued = cs + 1;
+            }
+            if (sm.abort && issued > 0) mbar_wait(&sm.v_full, (issued - 1) & 1, err, nullptr);
+        } else if (lane == 1) {
+            // -------------------------------------------------------- output store (lane 1)
+            for (int u = 0;; ++u) {
+                const int slot = u % kRing;
+                if (!mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort)) break;
+                const volatile TileDesc &d = sm.desc[slot];
+                const int flags = d.flags;
+                if (flags & kFlagEnd) break;
+                const int ent0 = d.ent0, n_valid = d.n_valid;
+                mbar_arrive(&sm.desc_empty[slot]);
+                if (!mbar_wait(&sm.stg_full, u & 1, err, &sm.abort)) break;
+                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 in power-of-two boxes
+                int r0 = 0;
+                const int rows = n_valid * HPG;
+#pragma unroll
+                for (int b = 0; b < kStoreBoxes; ++b) {
+                    const int R = 128 >> b;
+                    if (rows & R) {
+#pragma unroll
+                        for (int i = 0; i < NSUB; ++i)
+                            tma_store_2d(&omaps.box[b], sm.stg + i * 16384 + r0 * 128, i * 64, ent0 * HPG + r0);
+                        r0 += R;
+                    }
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(&sm.stg_free);
+            }
+            bulk_wait_all();
+        }
+    } else if (warp == 2) {
         // ------------------------------------------------------------ Q loader
         int n_q = 0;        // tiles whose Q copies were issued
         int ends = 0;
         for (int u = 0; ends < 2; ++u) {
             const int slot = u % kRing;
             // every lane waits (acquires) before it reads the descriptor
-            bool w = __all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort));
-            if (!w) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort))) break;
             const volatile TileDesc &d = sm.desc[slot];
             if (d.flags & kFlagEnd) {
                 ++ends;
@@ -356,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             }
             const int qb = n_q & 1;
             if (n_q >= 2) {
+                bool w = true;
                 if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((n_q >> 1) - 1) & 1, err, &sm.abort);
                 if (!__shfl_sync(0xffffffffu, w, 0)) break;
             }
@@ -380,16 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int u = 0, cs = -1;
+            int u = 0, cs_k = -1, cs_v = -1;
             bool have_prev = false;
             int p_u = 0, p_flags = 0;
             auto do_pv = [&](int t, int flags) -> bool {
                 const int b = t & 1;
                 if (!mbar_wait(&sm.p_full[b], (t >> 1) & 1, err, &sm.abort)) return false;
                 if (t >= 2 && !mbar_wait(&sm.o_free[b], ((t >> 1) - 1) & 1, err, &sm.abort)) return false;
+                if (flags & kFlagFirst) {
+                    ++cs_v;
+                    if (!mbar_wait(&sm.v_full, cs_v & 1, err, &sm.abort)) return false;
+                }
                 tc_fence_after();
-                const int kvb = flags & kFlagKv1;
-                const uint32_t v_addr = smem_u32(sm.v[kvb]);
+                const uint32_t v_addr = smem_u32(sm.v);
 #pragma unroll
                 for (int kt = 0; kt < 8; ++kt) {
                     const uint64_t bd = make_smem_desc(v_addr + uint32_t(kt * 2048), 16384, 1024, 2);
@@ -397,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                                 kt > 0 ? 1u : 0u);
                 }
                 mma_commit(&sm.o_full[b]);
-                if (flags & kFlagLast) mma_commit(&sm.kv_empty[kvb]);
+                if (flags & kFlagLast) mma_commit(&sm.v_empty);
                 return true;
             };
             for (;;) {
@@ -406,15 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
                 if (flags & kFlagEnd) break;
                 mbar_arrive(&sm.desc_empty[slot]);
-                const int kvb = flags & kFlagKv1;
+                const int kb = flags & kFlagKv1;
                 if (flags & kFlagFirst) {
-                    ++cs;
-                    if (!mbar_wait(&sm.kv_full[kvb], (cs >> 1) & 1, err, &sm.abort)) break;
+                    ++cs_k;
+                    if (!mbar_wait(&sm.k_full[kb], (cs_k >> 1) & 1, err, &sm.abort)) break;
                 }
                 const int b = u & 1;
                 if (!mbar_wait(&sm.q_full[b], (u >> 1) & 1, err, &sm.abort)) break;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(sm.q[b]), k_addr = smem_u32(sm.k[kvb]);
+                const uint32_t q_addr = smem_u32(sm.q[b]), k_addr = smem_u32(sm.k[kb]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = uint32_t((kk >> 2) * 16384 + (kk & 3) * 32);
@@ -423,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 }
                 mma_commit(&sm.s_full[b]);
                 mma_commit(&sm.q_empty[b]);
+                if (flags & kFlagLast) mma_commit(&sm.k_empty[kb]);
                 if (have_prev && !do_pv(p_u, p_flags)) {
                     have_prev = false;
                     break;
@@ -436,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
-    } else if (warp >= 2 && warp < 10) {
-        // ------------------------------------------------------------ softmax groups
-        const int wg = (warp - 2) >> 2;
+    } else {
+        // ------------------------------------------------------------ softmax groups (warps 4-11)
+        const int wg = (warp - 4) >> 2;
         const int quad = warp & 3;                 // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const int e = row / HPG, h = row - (row / HPG) * HPG;
@@ -460,50 +541,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
-            float s[128];
-            {
-                uint32_t v[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(t_s + uint32_t(c * 32), v[c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
-            }
-            // row max as eight independent chains
+            // pass 1: row max over the visible tokens (32-column chunks; loops kept rolled so the
+            // code stays small enough for the instruction cache of a 12-warp CTA)
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-            if (lim >= 127) {
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(t_s + uint32_t(c), v);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    s[c] = c <= lim ? s[c] : -INFINITY;
-                    mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-                }
+                for (int i = 0; i < 32; ++i)
+                    mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
             }
             const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float ms = m * scale;
-            // probabilities 2^(s*scale - ms) as packed bf16 into TMEM; their fp32 sum in eight
-            // chains normalises O and gives the lse
+            // pass 2: probabilities 2^(s*scale - ms) as packed bf16 over the columns already read
+            // (P of chunk c lands in columns c/2 .. c/2+15, below the chunks still to read); their
+            // fp32 sum in eight chains normalises O and gives the lse
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(t_s + uint32_t(c), v);
+                tmem_ld_wait();
+                uint32_t w[16];
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 64) {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float pa = fast_exp2(fmaf(s[c0 + 2 * i], scale, -ms));
-                    const float pb = fast_exp2(fmaf(s[c0 + 2 * i + 1], scale, -ms));
+                for (int i = 0; i < 16; ++i) {
+                    const float sa = (c + 2 * i <= lim) ? __uint_as_float(v[2 * i]) : -INFINITY;
+                    const float sb = (c + 2 * i + 1 <= lim) ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
+                    const float pa = fast_exp2(fmaf(sa, scale, -ms));
+                    const float pb = fast_exp2(fmaf(sb, scale, -ms));
                     w[i] = pack_bf16x2(pa, pb);
                     acc[i & 7] += pa + pb;
                 }
-                tmem_st32(t_s + uint32_t(c0 >> 1), w);
+                tmem_st16(t_s + uint32_t(c >> 1), w);
             }
             const float le = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             tmem_st_wait();
@@ -511,31 +587,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full[wg]);
 
+            // epilogue: O chunk by chunk, normalised, into the staging buffer
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, &sm.abort))) break;
+            if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free, (u - 1) & 1, err, &sm.abort))) break;
             tc_fence_after();
-            uint32_t ov[D / 32][32];
+            const float inv = 1.0f / le;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(t_o + uint32_t(c), o);
+                tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + uint32_t(c * 32), ov[c]);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.o_free[wg]);
-            if (qq >= 0) {
-                const float inv = 1.0f / le;
-                const size_t unit = size_t(idx) * HPG + h;
-                uint16_t *dst = o_part + unit * D;
-#pragma unroll
-                for (int i = 0; i < D; i += 8) {
-                    const uint32_t *o8 = &ov[i >> 5][i & 31];
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(o8[0]) * inv, __uint_as_float(o8[1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(o8[2]) * inv, __uint_as_float(o8[3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(o8[4]) * inv, __uint_as_float(o8[5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(o8[6]) * inv, __uint_as_float(o8[7]) * inv);
-                    *reinterpret_cast<uint4 *>(dst + i) = w;
+                for (int i = 0; i < 32; i += 8) {
+                    const int cc = ((c + i) >> 3) & 7;
+                    const uint32_t addr =
+                        smem_u32(sm.stg + ((c + i) >> 6) * 16384 + row * 128 + ((cc ^ (row & 7)) << 4));
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "r"(pack_bf16x2(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv)),
+                                 "r"(pack_bf16x2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv)),
+                                 "r"(pack_bf16x2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv)),
+                                 "r"(pack_bf16x2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv))
+                                 : "memory");
                 }
-                lse_part[unit] = (ms + log2f(le)) * kLn2;
             }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.o_free[wg]);
+                mbar_arrive(&sm.stg_full);
+            }
+            if (qq >= 0) lse_part[size_t(idx) * HPG + h] = (ms + log2f(le)) * kLn2;
         }
     }
 
@@ -565,6 +647,7 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
                      int n_pages, const Shape &s, void *o_part, float *lse_part, void *ws, int32_t *err,
                      cudaStream_t st) {
     alignas(64) CUtensorMap qm, km, vm;
+    alignas(64) StoreMaps om;
     const char *why = nullptr;
     {
         const uint64_t dims[3] = {uint64_t(D), uint64_t(s.Hq), uint64_t(n_rows)};
@@ -579,6 +662,15 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
         if (!encode_tensor_map(&km, 4, k_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
         if (!encode_tensor_map(&vm, 4, v_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
     }
+    {
+        // partials [n_rows * G * topk * HPG rows][D], row = entry * HPG + head
+        const uint64_t dims[2] = {uint64_t(D), uint64_t(n_rows) * uint64_t(s.G) * uint64_t(s.topk) * HPG};
+        const uint64_t strides[1] = {uint64_t(D) * 2};
+        for (int b = 0; b < kStoreBoxes; ++b) {
+            const uint32_t box[2] = {64u, uint32_t(128 >> b)};
+            if (!encode_tensor_map(&om.box[b], 2, o_part, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
+        }
+    }
     const long long n_keys = 1LL * s.G * n_req * s.max_blocks;
     if (n_keys > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
     const PlanLayout pl = plan_layout(n_rows, n_req, s);
@@ -591,9 +683,8 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
     e = cudaFuncSetAttribute(k_attn_prefill<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true, qm, km,
-                         vm, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows, n_req,
-                         n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, static_cast<uint16_t *>(o_part), lse_part,
-                         err);
+                         vm, om, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows,
+                         n_req, n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, lse_part, err);
 }
 
 }  // namespace
