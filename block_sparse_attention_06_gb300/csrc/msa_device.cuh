@@ -97,12 +97,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // Suspension granted per try while waiting (the waiting warp issues nothing meanwhile).
 constexpr uint32_t kWaitSleepNs = 20000;   // 20 us
 
+// The slow path of mbar_wait, out of line: one copy of the polling loop serves
+// every call site, which keeps warp-specialised kernels small for the
+// instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *err, volatile int *abort);
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs, raising MSA_FLAG_TIMEOUT and setting *abort; returns false then.
 // Returns false at once when *abort is already set by another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
                                           volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, abort);
+}
+
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *err, volatile int *abort) {
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
