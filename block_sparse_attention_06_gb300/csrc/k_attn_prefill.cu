@@ -17,17 +17,18 @@
 // written in CSR-entry order, so the output of one tile is one contiguous block.
 //
 // One CTA (12 warps):
-//   warp 0     decoder: takes chunks, loads K_j by TMA (128B swizzle, 64-column
-//              boxes) into one of two K buffers, warms L2 with V_j and hands the
-//              chunk to the V loader, and decodes a whole chunk's entries (query
-//              row, slot, causal limit) at once, with the loads batched, into a
-//              ring of tile descriptors;
-//   warp 3     lane 0, V loader: V_j by TMA into the V buffer once the previous
-//              chunk's last PV has completed; lane 1, output store: the staged
-//              tile goes to the partials by TMA bulk tensor stores in a few
-//              power-of-two row boxes, then the staging buffer is handed on;
+//   warp 0     decoder: takes chunks, warms L2 with their K_j and V_j, hands
+//              each chunk to the K/V loader, and decodes a whole chunk's entries
+//              (query row, slot, causal limit) at once, with the loads batched,
+//              into a ring of tile descriptors;
+//   warp 3     lane 0, K/V loader: K_j by TMA (128B swizzle, 64-column boxes)
+//              once the previous chunk's last S has completed, V_j once its last
+//              PV has; lane 1, output store: the staged tile is one contiguous
+//              block of the CSR-ordered partials and leaves by TMA bulk tensor
+//              stores in a few power-of-two row boxes, then the staging buffer is
+//              handed to the next tile's softmax group;
 //   warp 2     Q loader: gathers the HPG heads of each entry's query row by TMA
-//              into one of two Q buffers;
+//              into one of three Q buffers;
 //   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
 //              K = D) into the S buffer of the tile's softmax group, then, once P
 //              is back in TMEM, O = P V with P as the TMEM A operand and V as an
@@ -49,11 +50,11 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kChunkTiles = 8;   // tiles per work chunk
 constexpr int kRing = 16;        // tile descriptors in flight (two chunks)
+constexpr int kQBuf = 3;         // Q buffers
 constexpr int kStoreBoxes = 6;   // store boxes of 128, 64, 32, 16, 8, 4 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kFlagKv1 = 1;      // K buffer 1 (else 0)
 constexpr int kFlagFirst = 2;    // first tile of its chunk
 constexpr int kFlagLast = 4;     // last tile of its chunk
 constexpr int kFlagEnd = 8;      // no more work
@@ -70,16 +71,19 @@ struct TileDesc {
 
 template <int D>
 struct AttnSmem {
-    alignas(1024) uint8_t k[2][D * 128 * 2];
+    alignas(1024) uint8_t k[D * 128 * 2];
     alignas(1024) uint8_t v[D * 128 * 2];
-    alignas(1024) uint8_t q[2][128 * D * 2];
+    alignas(1024) uint8_t q[kQBuf][128 * D * 2];
     alignas(1024) uint8_t stg[128 * D * 2];         // one tile's bf16 output on its way to the partials
     TileDesc desc[kRing];
-    int32_t chunk_page[4], chunk_g[4];              // decoder -> V loader
-    uint64_t k_full[2], k_empty[2], v_full, v_empty;
-    uint64_t q_full[2], q_empty[2];
+    int32_t chunk_page[4], chunk_g[4];              // decoder -> K/V loader
+    uint64_t k_full, k_empty, v_full, v_empty;
+    uint64_t q_full[kQBuf], q_empty[kQBuf];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-    uint64_t stg_full, stg_free;
+    // staging buffer written (one phase per tile), and free for the next writer: one barrier per
+    // softmax group (tile parity), so that no waiter can be two phases ahead of the barrier it
+    // watches (a group may run two tiles ahead of the store)
+    uint64_t stg_full, stg_free[2];
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
     uint64_t drain;
@@ -187,11 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     const long long cap = 1LL * n_rows * G * topk;
 
     if (tid == 0) {
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.k_full[b], 1);
-            mbar_init(&sm.k_empty[b], 1);
+        for (int b = 0; b < kQBuf; ++b) {
             mbar_init(&sm.q_full[b], 1);
             mbar_init(&sm.q_empty[b], 1);
+        }
+        mbar_init(&sm.k_full, 1);
+        mbar_init(&sm.k_empty, 1);
+        for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);
             mbar_init(&sm.p_full[b], 4);
             mbar_init(&sm.o_full[b], 1);
@@ -200,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.v_empty, 1);
         mbar_init(&sm.stg_full, 4);
-        mbar_init(&sm.stg_free, 1);
+        mbar_init(&sm.stg_free[0], 1);
+        mbar_init(&sm.stg_free[1], 1);
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.desc_ready[r], 32);
             mbar_init(&sm.desc_full[r], 32);
@@ -270,17 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const int end = min(end0, off + ENT_MAX);
             if (off >= end) continue;
             const int nt = (end - off + EPT - 1) / EPT;
-            const int kb = cs & 1;
-            // K into buffer kb once the last S of chunk cs-2 has completed; V warms L2 for the V loader
-            if (cs >= 2 && !wait_lane0(&sm.k_empty[kb], ((cs >> 1) - 1) & 1)) {
-                ok = false;
-                break;
-            }
+            // the K/V loader fetches this block after the chunks before it: warm L2 now
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sm.k_full[kb], D * 128 * 2);
 #pragma unroll
                 for (int i = 0; i < NSUB; ++i) {
-                    tma_load_4d(sm.k[kb] + i * 16384, &kmap, &sm.k_full[kb], i * 64, g, 0, page);
+                    tma_prefetch_l2_4d(&kmap, i * 64, g, 0, page);
                     tma_prefetch_l2_4d(&vmap, i * 64, g, 0, page);
                 }
             }
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             }
             if (lane < nt) {
                 TileDesc &d = sm.desc[(u + lane) % kRing];
-                d.flags = (kb ? kFlagKv1 : 0) | (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
+                d.flags = (lane == 0 ? kFlagFirst : 0) | (lane == nt - 1 ? kFlagLast : 0);
                 d.g = g;
                 d.ent0 = off + lane * EPT;
                 d.n_valid = min(EPT, end - (off + lane * EPT));
@@ -365,27 +366,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 mbar_arrive(&sm.chunk_ready[cs & 3]);
             }
         }
-        if (sm.abort && lane == 0) {
-            // drain: the K copies still in flight land before the CTA exits
-            for (int t = max(0, cs - 2); t < cs; ++t) mbar_wait(&sm.k_full[t & 1], (t >> 1) & 1, err, nullptr);
-        }
     } else if (warp == 3) {
-        // ------------------------------------------------------------ V loader (lane 0)
+        // ------------------------------------------------------------ K/V loader (lane 0)
         if (lane == 0) {
-            int issued = 0;
+            int n_k = 0, n_v = 0;   // copies issued
             for (int cs = 0;; ++cs) {
                 if (!mbar_wait(&sm.chunk_ready[cs & 3], (cs >> 2) & 1, err, &sm.abort)) break;
                 const int page = *reinterpret_cast<volatile int32_t *>(&sm.chunk_page[cs & 3]);
                 const int g = *reinterpret_cast<volatile int32_t *>(&sm.chunk_g[cs & 3]);
                 mbar_arrive(&sm.chunk_free[cs & 3]);
                 if (page < 0) break;
+                // K once the previous chunk's last S has completed, V once its last PV has
+                if (cs >= 1 && !mbar_wait(&sm.k_empty, (cs - 1) & 1, err, &sm.abort)) break;
+                mbar_arrive_expect_tx(&sm.k_full, D * 128 * 2);
+#pragma unroll
+                for (int i = 0; i < NSUB; ++i) tma_load_4d(sm.k + i * 16384, &kmap, &sm.k_full, i * 64, g, 0, page);
+                n_k = cs + 1;
                 if (cs >= 1 && !mbar_wait(&sm.v_empty, (cs - 1) & 1, err, &sm.abort)) break;
                 mbar_arrive_expect_tx(&sm.v_full, D * 128 * 2);
 #pragma unroll
                 for (int i = 0; i < NSUB; ++i) tma_load_4d(sm.v + i * 16384, &vmap, &sm.v_full, i * 64, g, 0, page);
-                issued = cs + 1;
+                n_v = cs + 1;
             }
-            if (sm.abort && issued > 0) mbar_wait(&sm.v_full, (issued - 1) & 1, err, nullptr);
+            if (sm.abort) {   // drain: the copies still in flight land before the CTA exits
+                if (n_k > 0) mbar_wait(&sm.k_full, (n_k - 1) & 1, err, nullptr);
+                if (n_v > 0) mbar_wait(&sm.v_full, (n_v - 1) & 1, err, nullptr);
+            }
         } else if (lane == 1) {
             // -------------------------------------------------------- output store (lane 1)
             for (int u = 0;; ++u) {
@@ -397,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 const int ent0 = d.ent0, n_valid = d.n_valid;
                 mbar_arrive(&sm.desc_empty[slot]);
                 if (!mbar_wait(&sm.stg_full, u & 1, err, &sm.abort)) break;
-                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 in power-of-two boxes
+                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 of the CSR-ordered partials, one
+                // contiguous block, in power-of-two boxes
                 int r0 = 0;
                 const int rows = n_valid * HPG;
 #pragma unroll
@@ -412,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 }
                 bulk_commit();
                 bulk_wait_read_all();
-                mbar_arrive(&sm.stg_free);
+                mbar_arrive(&sm.stg_free[(u + 1) & 1]);   // for the writer of tile u + 1
             }
             bulk_wait_all();
         }
@@ -430,10 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 mbar_arrive(&sm.desc_full[slot]);
                 continue;
             }
-            const int qb = n_q & 1;
-            if (n_q >= 2) {
+            const int qb = n_q % kQBuf;
+            if (n_q >= kQBuf) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((n_q >> 1) - 1) & 1, err, &sm.abort);
+                if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((n_q / kQBuf) - 1) & 1, err, &sm.abort);
                 if (!__shfl_sync(0xffffffffu, w, 0)) break;
             }
             const int g = d.g;
@@ -452,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         }
         if (sm.abort && lane == 0) {
             // drain: the Q copies still in flight land before the CTA exits
-            for (int t = max(0, n_q - 2); t < n_q; ++t) mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, err, nullptr);
+            for (int t = max(0, n_q - kQBuf); t < n_q; ++t)
+                mbar_wait(&sm.q_full[t % kQBuf], (t / kQBuf) & 1, err, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -486,15 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
                 if (flags & kFlagEnd) break;
                 mbar_arrive(&sm.desc_empty[slot]);
-                const int kb = flags & kFlagKv1;
                 if (flags & kFlagFirst) {
                     ++cs_k;
-                    if (!mbar_wait(&sm.k_full[kb], (cs_k >> 1) & 1, err, &sm.abort)) break;
+                    if (!mbar_wait(&sm.k_full, cs_k & 1, err, &sm.abort)) break;
                 }
-                const int b = u & 1;
-                if (!mbar_wait(&sm.q_full[b], (u >> 1) & 1, err, &sm.abort)) break;
+                const int qb = u % kQBuf;
+                if (!mbar_wait(&sm.q_full[qb], (u / kQBuf) & 1, err, &sm.abort)) break;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(sm.q[b]), k_addr = smem_u32(sm.k[kb]);
+                const int b = u & 1;
+                const uint32_t q_addr = smem_u32(sm.q[qb]), k_addr = smem_u32(sm.k);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = uint32_t((kk >> 2) * 16384 + (kk & 3) * 32);
@@ -502,8 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                              make_smem_desc(k_addr + o, 16, 1024, 2), kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&sm.s_full[b]);
-                mma_commit(&sm.q_empty[b]);
-                if (flags & kFlagLast) mma_commit(&sm.k_empty[kb]);
+                mma_commit(&sm.q_empty[qb]);
+                if (flags & kFlagLast) mma_commit(&sm.k_empty);
                 if (have_prev && !do_pv(p_u, p_flags)) {
                     have_prev = false;
                     break;
@@ -589,7 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
             // epilogue: O chunk by chunk, normalised, into the staging buffer
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, &sm.abort))) break;
-            if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free, (u - 1) & 1, err, &sm.abort))) break;
+            // the staging buffer is free once tile u - 1 has left it (the ((u - 1) / 2)-th release on
+            // this group's barrier)
+            if (u >= 1 &&
+                !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free[u & 1], ((u - 1) >> 1) & 1, err, &sm.abort)))
+                break;
             tc_fence_after();
             const float inv = 1.0f / le;
 #pragma unroll 1
@@ -611,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 }
             }
             tc_fence_before();
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();   // the staged rows are read by the TMA engine
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.o_free[wg]);
