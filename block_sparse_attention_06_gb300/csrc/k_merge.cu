@@ -20,8 +20,9 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
                                                    const int32_t *__restrict__ ent_pos, int Hq, int G,
                                                    int topk, long long n_ent, uint16_t *__restrict__ out,
                                                    float *__restrict__ lse, int32_t *err) {
-    extern __shared__ float sh[];   // w_s [topk][Hq] weights exp(lse_s - lse) (0 for empty slots),
-                                    // then pos_s [G][topk] entry of each (group, slot), -1 if empty
+    extern __shared__ float sh[];   // w_s [topk][Hq]: each slot's lse, then its weight exp(lse_s - lse)
+                                    // (0 for empty slots); pos_s [G][topk] entry of each (group, slot),
+                                    // -1 if empty
     float *w_s = sh;
     int32_t *pos_s = reinterpret_cast<int32_t *>(sh + topk * Hq);
     const int q = blockIdx.x;
@@ -40,22 +41,30 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
         pos_s[i] = p;
     }
     __syncthreads();
-    for (int h = tid; h < Hq; h += blockDim.x) {
+    // every (slot, head) lse of the row into shared memory, all loads independent
+    for (int i = tid; i < topk * Hq; i += blockDim.x) {
+        const int s = i / Hq, h = i - (i / Hq) * Hq;
         const int g = h / hpg, hh = h - g * hpg;
-        const int32_t *ps = pos_s + g * topk;
+        const int p = pos_s[g * topk + s];
+        w_s[i] = p >= 0 ? lse_part[size_t(p) * hpg + hh] : -INFINITY;
+    }
+    __syncthreads();
+    for (int h = tid; h < Hq; h += blockDim.x) {
         float m = -INFINITY;
-        for (int s = 0; s < topk; ++s)
-            if (ps[s] >= 0) m = fmaxf(m, lse_part[size_t(ps[s]) * hpg + hh]);
+        for (int s = 0; s < topk; ++s) m = fmaxf(m, w_s[s * Hq + h]);
         float tot = -INFINITY;
         if (m != -INFINITY) {
             float sum = 0.f;
-            for (int s = 0; s < topk; ++s)
-                if (ps[s] >= 0) sum += __expf(lse_part[size_t(ps[s]) * hpg + hh] - m);
+            for (int s = 0; s < topk; ++s) {
+                const float l = w_s[s * Hq + h];
+                if (l != -INFINITY) sum += __expf(l - m);
+            }
             tot = m + __logf(sum);
         }
-        for (int s = 0; s < topk; ++s)
-            w_s[s * Hq + h] = (ps[s] >= 0 && tot != -INFINITY) ? __expf(lse_part[size_t(ps[s]) * hpg + hh] - tot)
-                                                               : 0.f;
+        for (int s = 0; s < topk; ++s) {
+            const float l = w_s[s * Hq + h];
+            w_s[s * Hq + h] = (l != -INFINITY && tot != -INFINITY) ? __expf(l - tot) : 0.f;
+        }
         lse[size_t(q) * Hq + h] = tot;
     }
     __syncthreads();
@@ -65,19 +74,30 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
         const int g = h / hpg, hh = h - g * hpg;
         const int col = (c - h * (D / 8)) * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < topk; ++s) {
-            const float w = w_s[s * Hq + h];
-            if (w == 0.f) continue;   // empty slot: its partial was never written
-            const uint4 v = *reinterpret_cast<const uint4 *>(
-                o_part + (size_t(pos_s[g * topk + s]) * hpg + hh) * D + col);
-            acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
-            acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
-            acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
-            acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
-            acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
-            acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
-            acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
-            acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+        // four slots' loads in flight at a time; an empty slot (weight 0, never written) reads
+        // entry 0 instead and is left out by a select, so no stale value can reach the sum
+        for (int s0 = 0; s0 < topk; s0 += 4) {
+            uint4 v[4];
+            float w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int s = s0 + i;
+                w[i] = s < topk ? w_s[s * Hq + h] : 0.f;
+                const int p = (s < topk && w[i] != 0.f) ? pos_s[g * topk + s] : 0;
+                v[i] = *reinterpret_cast<const uint4 *>(o_part + (size_t(p) * hpg + hh) * D + col);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (w[i] == 0.f) continue;
+                acc[0] = fmaf(w[i], bf16_lo(v[i].x), acc[0]);
+                acc[1] = fmaf(w[i], bf16_hi(v[i].x), acc[1]);
+                acc[2] = fmaf(w[i], bf16_lo(v[i].y), acc[2]);
+                acc[3] = fmaf(w[i], bf16_hi(v[i].y), acc[3]);
+                acc[4] = fmaf(w[i], bf16_lo(v[i].z), acc[4]);
+                acc[5] = fmaf(w[i], bf16_hi(v[i].z), acc[5]);
+                acc[6] = fmaf(w[i], bf16_lo(v[i].w), acc[6]);
+                acc[7] = fmaf(w[i], bf16_hi(v[i].w), acc[7]);
+            }
         }
         uint4 r;
         r.x = pack_bf16x2(acc[0], acc[1]);

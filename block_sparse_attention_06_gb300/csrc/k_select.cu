@@ -463,13 +463,20 @@ cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, c
     if (items <= 0) return cudaSuccess;
     const int mb = s.max_blocks;
     if (mb <= 1024) {
+        // keys per lane in steps of 4: no lane holds more empty slots than it must
         const unsigned grid = unsigned((items + 7) / 8);
-        if (mb <= 128)
-            k_topk_warp<4><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
-        else if (mb <= 512)
-            k_topk_warp<16><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
-        else
-            k_topk_warp<32><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err);
+        const int per = (mb + 31) / 32;
+#define MSA_TOPK_WARP(P) \
+    k_topk_warp<P><<<grid, 256, 0, st>>>(scores, q_pos, n_rows, s.G, mb, s.topk, sel, err)
+        if (per <= 4) MSA_TOPK_WARP(4);
+        else if (per <= 8) MSA_TOPK_WARP(8);
+        else if (per <= 12) MSA_TOPK_WARP(12);
+        else if (per <= 16) MSA_TOPK_WARP(16);
+        else if (per <= 20) MSA_TOPK_WARP(20);
+        else if (per <= 24) MSA_TOPK_WARP(24);
+        else if (per <= 28) MSA_TOPK_WARP(28);
+        else MSA_TOPK_WARP(32);
+#undef MSA_TOPK_WARP
     } else if (mb <= 8192) {
         k_topk_cta<256, 32><<<unsigned(items), 256, 0, st>>>(scores, q_pos, s.G, mb, s.topk, sel, err);
     } else if (mb <= 16384) {
