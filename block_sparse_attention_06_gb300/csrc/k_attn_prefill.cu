@@ -559,9 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 uint32_t v[32];
                 tmem_ld32(t_s + uint32_t(c), v);
                 tmem_ld_wait();
+                if (c + 31 <= lim) {   // fully visible chunk (every block but a row's own one)
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                    for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                }
             }
             const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -578,14 +583,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 tmem_ld32(t_s + uint32_t(c), v);
                 tmem_ld_wait();
                 uint32_t w[16];
+                if (c + 31 <= lim) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float sa = (c + 2 * i <= lim) ? __uint_as_float(v[2 * i]) : -INFINITY;
-                    const float sb = (c + 2 * i + 1 <= lim) ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
-                    const float pa = fast_exp2(fmaf(sa, scale, -ms));
-                    const float pb = fast_exp2(fmaf(sb, scale, -ms));
-                    w[i] = pack_bf16x2(pa, pb);
-                    acc[i & 7] += pa + pb;
+                    for (int i = 0; i < 16; ++i) {
+                        const float pa = fast_exp2(fmaf(__uint_as_float(v[2 * i]), scale, -ms));
+                        const float pb = fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), scale, -ms));
+                        w[i] = pack_bf16x2(pa, pb);
+                        acc[i & 7] += pa + pb;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float sa = (c + 2 * i <= lim) ? __uint_as_float(v[2 * i]) : -INFINITY;
+                        const float sb = (c + 2 * i + 1 <= lim) ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
+                        const float pa = fast_exp2(fmaf(sa, scale, -ms));
+                        const float pb = fast_exp2(fmaf(sb, scale, -ms));
+                        w[i] = pack_bf16x2(pa, pb);
+                        acc[i & 7] += pa + pb;
+                    }
                 }
                 tmem_st16(t_s + uint32_t(c >> 1), w);
             }
