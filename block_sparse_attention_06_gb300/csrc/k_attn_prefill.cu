@@ -16,29 +16,35 @@
 // queries is spread over many SMs while its K/V stays in L2.  Partials are
 // written in CSR-entry order, so the output of one tile is one contiguous block.
 //
-// One CTA (12 warps):
+// One CTA (19 warps):
 //   warp 0     decoder: takes chunks, warms L2 with their K_j and V_j, hands
 //              each chunk to the K/V loader, and decodes a whole chunk's entries
 //              (query row, slot, causal limit) at once, with the loads batched,
 //              into a ring of tile descriptors;
-//   warp 3     lane 0, K/V loader: K_j by TMA (128B swizzle, 64-column boxes)
-//              once the previous chunk's last S has completed, V_j once its last
-//              PV has; lane 1, output store: the staged tile is one contiguous
-//              block of the CSR-ordered partials and leaves by TMA bulk tensor
-//              stores in a few power-of-two row boxes, then the staging buffer is
-//              handed to the next tile's softmax group;
-//   warp 2     Q loader: gathers the HPG heads of each entry's query row by TMA
-//              into one of three Q buffers;
 //   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
 //              K = D) into the S buffer of the tile's softmax group, then, once P
 //              is back in TMEM, O = P V with P as the TMEM A operand and V as an
 //              MN-major shared-memory B operand;
+//   warp 2     K/V loader: K_j by TMA (128B swizzle, 64-column boxes) once the
+//              previous chunk's last S has completed, V_j once its last PV has;
+//   warp 3     output store: the staged tile is one contiguous block of the
+//              CSR-ordered partials and leaves by TMA bulk tensor stores in a few
+//              power-of-two row boxes;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
 //              from TMEM in 32-column chunks twice (row max, then exp2 and P as
-//              packed bf16 written over S), then O chunk by chunk, normalised,
-//              into the shared staging buffer in the 128B-swizzled box layout;
-//              while one group runs its softmax the tensor core works on the
-//              other group's tile.
+//              packed bf16 written over S); the row's 1/sum goes to shared
+//              memory and its lse to the partials; while one group runs its
+//              softmax the tensor core works on the other group's tile;
+//   warps 12-15  epilogue: every tile in order, O chunk by chunk from TMEM,
+//              normalised, into the shared staging buffer in the 128B-swizzled
+//              box layout, so a softmax group goes on to its next tile as soon
+//              as its P is in TMEM;
+//   warps 16-18  Q loaders, one per Q buffer, one tile each in turn: the HPG
+//              heads of each entry's query row (HPG * D * 2 contiguous bytes) by
+//              16-byte cp.async, in the 128B-swizzled layout the MMA reads.  One
+//              instruction moves 512 contiguous bytes, where a TMA box of the
+//              swizzled layout can move only 8 rows of 128 bytes.  A buffer has
+//              one loader, so its barriers' phases are waited in order.
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D of 512 columns).
 // Every wait is bounded; a timeout raises MSA_FLAG_TIMEOUT and every role drains.
 #include "msa_device.cuh"
@@ -47,7 +53,7 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 608;
 constexpr int kChunkTiles = 8;   // tiles per work chunk
 constexpr int kRing = 16;        // tile descriptors in flight (two chunks)
 constexpr int kQBuf = 3;         // Q buffers
@@ -76,14 +82,13 @@ struct AttnSmem {
     alignas(1024) uint8_t q[kQBuf][128 * D * 2];
     alignas(1024) uint8_t stg[128 * D * 2];         // one tile's bf16 output on its way to the partials
     TileDesc desc[kRing];
+    float inv_le[2][128];                           // 1 / row sum of P, per S/O buffer (softmax -> epilogue)
     int32_t chunk_page[4], chunk_g[4];              // decoder -> K/V loader
     uint64_t k_full, k_empty, v_full, v_empty;
     uint64_t q_full[kQBuf], q_empty[kQBuf];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-    // staging buffer written (one phase per tile), and free for the next writer: one barrier per
-    // softmax group (tile parity), so that no waiter can be two phases ahead of the barrier it
-    // watches (a group may run two tiles ahead of the store)
-    uint64_t stg_full, stg_free[2];
+    uint64_t stat_free[2];                          // inv_le[b] read by the epilogue
+    uint64_t stg_full, stg_free;                    // staging buffer written / read by the store (one phase per tile)
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
     uint64_t drain;
@@ -173,7 +178,7 @@ struct StoreMaps {
 
 template <int D, int HPG>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
-    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const uint8_t *__restrict__ qg, int Hq, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ StoreMaps omaps,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos,
     const int32_t *__restrict__ blk_off, const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr,
@@ -202,16 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mbar_init(&sm.p_full[b], 4);
             mbar_init(&sm.o_full[b], 1);
             mbar_init(&sm.o_free[b], 4);
+            mbar_init(&sm.stat_free[b], 4);
         }
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.v_empty, 1);
         mbar_init(&sm.stg_full, 4);
-        mbar_init(&sm.stg_free[0], 1);
-        mbar_init(&sm.stg_free[1], 1);
+        mbar_init(&sm.stg_free, 1);
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.desc_ready[r], 32);
-            mbar_init(&sm.desc_full[r], 32);
-            mbar_init(&sm.desc_empty[r], 6);
+            mbar_init(&sm.desc_full[r], 1);   // the tile's Q loader, once it has read the descriptor
+            mbar_init(&sm.desc_empty[r], 10);   // MMA, store, a softmax group's 4 warps, the epilogue's 4
         }
         for (int r = 0; r < 4; ++r) {
             mbar_init(&sm.chunk_ready[r], 1);
@@ -226,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         for (int i = 0; i < kStoreBoxes; ++i) tma_prefetch_desc(&omaps.box[i]);
@@ -352,8 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             for (int t = 0; t < nt; ++t) mbar_arrive(&sm.desc_ready[(u + t) % kRing]);
             u += nt;
         }
-        // end markers: two tiles (one per softmax group; the MMA and store warps stop at the first), one chunk
-        for (int e = 0; ok && e < 2; ++e) {
+        // end markers: three tiles (one per Q loader, and so one per softmax group; the MMA, store and
+        // epilogue warps stop at the first), one chunk
+        for (int e = 0; ok && e < kQBuf; ++e) {
             const int slot = u % kRing;
             if (u >= kRing && !wait_lane0(&sm.desc_empty[slot], ((u / kRing) - 1) & 1)) break;
             if (lane == 0) sm.desc[slot].flags = kFlagEnd;
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 mbar_arrive(&sm.chunk_ready[cs & 3]);
             }
         }
-    } else if (warp == 3) {
+    } else if (warp == 2) {
         // ------------------------------------------------------------ K/V loader (lane 0)
         if (lane == 0) {
             int n_k = 0, n_v = 0;   // copies issued
@@ -392,8 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (n_k > 0) mbar_wait(&sm.k_full, (n_k - 1) & 1, err, nullptr);
                 if (n_v > 0) mbar_wait(&sm.v_full, (n_v - 1) & 1, err, nullptr);
             }
-        } else if (lane == 1) {
-            // -------------------------------------------------------- output store (lane 1)
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ output store (lane 0)
+        if (lane == 0) {
             for (int u = 0;; ++u) {
                 const int slot = u % kRing;
                 if (!mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort)) break;
@@ -419,48 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 }
                 bulk_commit();
                 bulk_wait_read_all();
-                mbar_arrive(&sm.stg_free[(u + 1) & 1]);   // for the writer of tile u + 1
+                mbar_arrive(&sm.stg_free);
             }
             bulk_wait_all();
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------------------ Q loader
-        int n_q = 0;        // tiles whose Q copies were issued
-        int ends = 0;
-        for (int u = 0; ends < 2; ++u) {
-            const int slot = u % kRing;
-            // every lane waits (acquires) before it reads the descriptor
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort))) break;
-            const volatile TileDesc &d = sm.desc[slot];
-            if (d.flags & kFlagEnd) {
-                ++ends;
-                mbar_arrive(&sm.desc_full[slot]);
-                continue;
-            }
-            const int qb = n_q % kQBuf;
-            if (n_q >= kQBuf) {
-                bool w = true;
-                if (lane == 0) w = mbar_wait(&sm.q_empty[qb], ((n_q / kQBuf) - 1) & 1, err, &sm.abort);
-                if (!__shfl_sync(0xffffffffu, w, 0)) break;
-            }
-            const int g = d.g;
-            const int qq = lane < EPT ? d.qq[lane] : -1;
-            if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qb], 128 * D * 2);
-            __syncwarp();
-            if (lane < EPT) {
-                const int row = qq >= 0 ? qq : n_rows;   // fully out of bounds -> zero rows
-#pragma unroll
-                for (int i = 0; i < NSUB; ++i)
-                    tma_load_3d(sm.q[qb] + i * 16384 + lane * HPG * 128, &qmap, &sm.q_full[qb], i * 64, g * HPG,
-                                row);
-            }
-            ++n_q;
-            mbar_arrive(&sm.desc_full[slot]);
-        }
-        if (sm.abort && lane == 0) {
-            // drain: the Q copies still in flight land before the CTA exits
-            for (int t = max(0, n_q - kQBuf); t < n_q; ++t)
-                mbar_wait(&sm.q_full[t % kQBuf], (t / kQBuf) & 1, err, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -525,7 +493,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
-    } else {
+    } else if (warp >= 16) {
+        // ------------------------------------------------------------ Q loaders (warps 16-18)
+        constexpr int CPH = D / 8;         // 16-byte chunks of one head row
+        constexpr int CPE = HPG * CPH;     // of one entry (a multiple of 32)
+        static_assert(CPE % 32 == 0, "an entry spans whole warps of 16-byte chunks");
+        // this lane's chunks of an entry: head and chunk column of chunk j * 32 + lane
+        const uint8_t *q_row0 = qg + size_t(lane % CPH) * 16;   // + head row offset below
+        const int qb = warp - 16;          // this warp's Q buffer: tiles u with u % kQBuf == qb
+        for (int u = qb;; u += kQBuf) {
+            const int slot = u % kRing;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort))) break;
+            const volatile TileDesc &d = sm.desc[slot];
+            if (d.flags & kFlagEnd) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.desc_full[slot]);
+                break;
+            }
+            if (u >= kQBuf &&
+                !__all_sync(0xffffffffu, mbar_wait(&sm.q_empty[qb], ((u / kQBuf) - 1) & 1, err, &sm.abort)))
+                break;
+            const int g = d.g;
+            const uint32_t qdst = smem_u32(sm.q[qb]);
+#pragma unroll 1
+            for (int e = 0; e < EPT; ++e) {
+                const int qq = d.qq[e];
+                const uint8_t *src = q_row0 + (size_t(qq) * Hq + size_t(g) * HPG) * (D * 2);
+#pragma unroll
+                for (int j = 0; j < CPE / 32; ++j) {
+                    const int c = j * 32 + lane;
+                    const int h = c / CPH, cw = c % CPH;
+                    const int r = e * HPG + h;   // row of the 128-row tile
+                    const uint32_t dst = qdst + uint32_t((cw >> 3) * 16384 + r * 128 + (((cw & 7) ^ (r & 7)) << 4));
+                    if (qq >= 0) {
+                        cp_async_16(dst, src + size_t(h) * (D * 2));
+                    } else {   // padding or rejected entry: zero rows
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                    }
+                }
+            }
+            cp_async_commit();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.desc_full[slot]);   // the descriptor has been read
+            cp_async_wait<0>();
+            fence_proxy_async_smem();   // the copied rows are read by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.q_full[qb]);
+        }
+        cp_async_wait<0>();   // nothing in flight when the CTA exits
+    } else if (warp < 12) {
         // ------------------------------------------------------------ softmax groups (warps 4-11)
         const int wg = (warp - 4) >> 2;
         const int quad = warp & 3;                 // TMEM lanes this warp may access
@@ -533,7 +549,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         const int e = row / HPG, h = row - (row / HPG) * HPG;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
         const uint32_t t_s = tmem + lane_off + uint32_t(wg * 128);
-        const uint32_t t_o = tmem + lane_off + uint32_t(256 + wg * D);
         const float scale = sm_scale * kLog2e;
         for (int u = wg;; u += 2) {
             const int slot = u % kRing;
@@ -550,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
             // pass 1: row max over the visible tokens (32-column chunks; loops kept rolled so the
-            // code stays small enough for the instruction cache of a 12-warp CTA)
+            // code stays small enough for the instruction cache of a 16-warp CTA)
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
@@ -605,20 +620,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 tmem_st16(t_s + uint32_t(c >> 1), w);
             }
             const float le = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            // inv_le[wg] is free once the epilogue has read it for this group's previous tile
+            if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stat_free[wg], (k - 1) & 1, err, &sm.abort)))
+                break;
+            sm.inv_le[wg][row] = 1.0f / le;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full[wg]);
-
-            // epilogue: O chunk by chunk, normalised, into the staging buffer
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[wg], k & 1, err, &sm.abort))) break;
-            // the staging buffer is free once tile u - 1 has left it (the ((u - 1) / 2)-th release on
-            // this group's barrier)
-            if (u >= 1 &&
-                !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free[u & 1], ((u - 1) >> 1) & 1, err, &sm.abort)))
-                break;
+            if (qq >= 0) lse_part[size_t(idx) * HPG + h] = (ms + log2f(le)) * kLn2;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 12-15)
+        const int quad = warp & 3;                 // TMEM lanes this warp may access
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        for (int u = 0;; ++u) {
+            const int slot = u % kRing;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort))) break;
+            const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
+            __syncwarp();
+            if (flags & kFlagEnd) break;
+            if (lane == 0) mbar_arrive(&sm.desc_empty[slot]);
+            const int b = u & 1, k = u >> 1;
+            const uint32_t t_o = tmem + lane_off + uint32_t(256 + b * D);
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[b], k & 1, err, &sm.abort))) break;
+            // P (and with it inv_le) of tile u is complete: this wait orders the read below
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[b], k & 1, err, &sm.abort))) break;
+            const float inv = sm.inv_le[b][row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.stat_free[b]);
+            // the staging buffer is free once tile u - 1 has left it
+            if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free, (u - 1) & 1, err, &sm.abort))) break;
             tc_fence_after();
-            const float inv = 1.0f / le;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
@@ -641,10 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             fence_proxy_async_smem();   // the staged rows are read by the TMA engine
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sm.o_free[wg]);
+                mbar_arrive(&sm.o_free[b]);
                 mbar_arrive(&sm.stg_full);
             }
-            if (qq >= 0) lse_part[size_t(idx) * HPG + h] = (ms + log2f(le)) * kLn2;
         }
     }
 
@@ -673,15 +706,9 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
                      const int32_t *q_pos, const int32_t *blk_off, const int32_t *blk_ent, int n_rows, int n_req,
                      int n_pages, const Shape &s, void *o_part, float *lse_part, void *ws, int32_t *err,
                      cudaStream_t st) {
-    alignas(64) CUtensorMap qm, km, vm;
+    alignas(64) CUtensorMap km, vm;
     alignas(64) StoreMaps om;
     const char *why = nullptr;
-    {
-        const uint64_t dims[3] = {uint64_t(D), uint64_t(s.Hq), uint64_t(n_rows)};
-        const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(s.Hq) * D * 2};
-        const uint32_t box[3] = {64u, uint32_t(HPG), 1u};
-        if (!encode_tensor_map(&qm, 3, q, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
-    }
     {
         const uint64_t dims[4] = {uint64_t(D), uint64_t(s.G), 128ull, uint64_t(n_pages)};
         const uint64_t strides[3] = {uint64_t(D) * 2, uint64_t(s.G) * D * 2, 128ull * s.G * D * 2};
@@ -709,7 +736,8 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
     const size_t smem = sizeof(AttnSmem<D>) + 1024;
     e = cudaFuncSetAttribute(k_attn_prefill<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true, qm, km,
+    return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true,
+                         static_cast<const uint8_t *>(q), s.Hq, km,
                          vm, om, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows,
                          n_req, n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, lse_part, err);
 }
