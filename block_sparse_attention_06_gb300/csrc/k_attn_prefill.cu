@@ -104,6 +104,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Three-input fp32 maximum (one instruction on sm_100-class SMs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Two fp32 lanes per instruction (the f32x2 datapath of sm_100-class SMs); b2 / c2 hold one value
+// in both halves.
+__device__ __forceinline__ uint64_t dup2(float x) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, uint64_t b2, uint64_t c2) {
+    asm("{\n\t.reg .b64 x, d;\n\tmov.b64 x, {%2, %3};\n\tfma.rn.f32x2 d, x, %4, %5;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "l"(b2), "l"(c2));
+}
+__device__ __forceinline__ void fmul2(float &d0, float &d1, float a0, float a1, uint64_t b2) {
+    asm("{\n\t.reg .b64 x, d;\n\tmov.b64 x, {%2, %3};\n\tmul.rn.f32x2 d, x, %4;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "l"(b2));
+}
+// acc2 += (a0, a1), lane-wise
+__device__ __forceinline__ void fadd2_acc(uint64_t &acc2, float a0, float a1) {
+    asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%1, %2};\n\tadd.rn.f32x2 %0, %0, x;\n\t}" : "+l"(acc2) : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ float sum2(uint64_t acc2) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc2));
+    return a + b;
+}
+
 // Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
 constexpr size_t kPlanHeaderBytes = 16;
 
@@ -435,6 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         if (lane == 0) {
             int u = 0, cs_k = -1, cs_v = -1;
             bool have_prev = false;
+            const uint64_t kd = make_smem_desc(smem_u32(sm.k), 16, 1024, 2);
+            const uint64_t vd = make_smem_desc(smem_u32(sm.v), 16384, 1024, 2);
             int p_u = 0, p_flags = 0;
             auto do_pv = [&](int t, int flags) -> bool {
                 const int b = t & 1;
@@ -445,13 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     if (!mbar_wait(&sm.v_full, cs_v & 1, err, &sm.abort)) return false;
                 }
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(sm.v);
+                const uint32_t d_o = tmem + uint32_t(256 + b * D), a_p = tmem + uint32_t(b * 128);
 #pragma unroll
-                for (int kt = 0; kt < 8; ++kt) {
-                    const uint64_t bd = make_smem_desc(v_addr + uint32_t(kt * 2048), 16384, 1024, 2);
-                    mma_bf16_ts(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128 + kt * 8), bd, kIdescO,
-                                kt > 0 ? 1u : 0u);
-                }
+                for (int kt = 0; kt < 8; ++kt)
+                    mma_bf16_ts(d_o, a_p + uint32_t(kt * 8), vd + uint64_t(kt * 2048 >> 4), kIdescO, kt > 0 ? 1u : 0u);
                 mma_commit(&sm.o_full[b]);
                 if (flags & kFlagLast) mma_commit(&sm.v_empty);
                 return true;
@@ -470,12 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (!mbar_wait(&sm.q_full[qb], (u / kQBuf) & 1, err, &sm.abort)) break;
                 tc_fence_after();
                 const int b = u & 1;
-                const uint32_t q_addr = smem_u32(sm.q[qb]), k_addr = smem_u32(sm.k);
+                const uint64_t qd = make_smem_desc(smem_u32(sm.q[qb]), 16, 1024, 2);
+                const uint32_t d_s = tmem + uint32_t(b * 128);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = uint32_t((kk >> 2) * 16384 + (kk & 3) * 32);
-                    mma_bf16(tmem + uint32_t(b * 128), make_smem_desc(q_addr + o, 16, 1024, 2),
-                             make_smem_desc(k_addr + o, 16, 1024, 2), kIdescS, kk > 0 ? 1u : 0u);
+                    // the descriptor's start-address field counts 16-byte units
+                    const uint64_t o = uint64_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    mma_bf16(d_s, qd + o, kd + o, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&sm.s_full[b]);
                 mma_commit(&sm.q_empty[qb]);
@@ -576,22 +610,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 tmem_ld_wait();
                 if (c + 31 <= lim) {   // fully visible chunk (every block but a row's own one)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(v[i]));
+                    for (int i = 0; i < 32; i += 16)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            mx[j] = fmax3(mx[j], __uint_as_float(v[i + j]), __uint_as_float(v[i + 8 + j]));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
                 }
             }
-            const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            const float m = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             const float ms = m * scale;
+            const uint64_t scale2 = dup2(scale), nms2 = dup2(-ms);
             // pass 2: probabilities 2^(s*scale - ms) as packed bf16 over the columns already read
             // (P of chunk c lands in columns c/2 .. c/2+15, below the chunks still to read); their
-            // fp32 sum in eight chains normalises O and gives the lse
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+            // fp32 sum in eight chains (four lane pairs) normalises O and gives the lse
+            uint64_t acc2[4] = {0, 0, 0, 0};
 #pragma unroll 1
             for (int c = 0; c < 128; c += 32) {
                 uint32_t v[32];
@@ -601,25 +636,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (c + 31 <= lim) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float pa = fast_exp2(fmaf(__uint_as_float(v[2 * i]), scale, -ms));
-                        const float pb = fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), scale, -ms));
+                        float xa, xb;
+                        ffma2(xa, xb, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), scale2, nms2);
+                        const float pa = fast_exp2(xa), pb = fast_exp2(xb);
                         w[i] = pack_bf16x2(pa, pb);
-                        acc[i & 7] += pa + pb;
+                        fadd2_acc(acc2[i & 3], pa, pb);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const float sa = (c + 2 * i <= lim) ? __uint_as_float(v[2 * i]) : -INFINITY;
                         const float sb = (c + 2 * i + 1 <= lim) ? __uint_as_float(v[2 * i + 1]) : -INFINITY;
-                        const float pa = fast_exp2(fmaf(sa, scale, -ms));
-                        const float pb = fast_exp2(fmaf(sb, scale, -ms));
+                        float xa, xb;
+                        ffma2(xa, xb, sa, sb, scale2, nms2);
+                        const float pa = fast_exp2(xa), pb = fast_exp2(xb);
                         w[i] = pack_bf16x2(pa, pb);
-                        acc[i & 7] += pa + pb;
+                        fadd2_acc(acc2[i & 3], pa, pb);
                     }
                 }
                 tmem_st16(t_s + uint32_t(c >> 1), w);
             }
-            const float le = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            const float le = (sum2(acc2[0]) + sum2(acc2[1])) + (sum2(acc2[2]) + sum2(acc2[3]));
             // inv_le[wg] is free once the epilogue has read it for this group's previous tile
             if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stat_free[wg], (k - 1) & 1, err, &sm.abort)))
                 break;
@@ -647,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[b], k & 1, err, &sm.abort))) break;
             // P (and with it inv_le) of tile u is complete: this wait orders the read below
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[b], k & 1, err, &sm.abort))) break;
-            const float inv = sm.inv_le[b][row];
+            const uint64_t inv2 = dup2(sm.inv_le[b][row]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.stat_free[b]);
             // the staging buffer is free once tile u - 1 has left it
@@ -663,11 +700,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     const int cc = ((c + i) >> 3) & 7;
                     const uint32_t addr =
                         smem_u32(sm.stg + ((c + i) >> 6) * 16384 + row * 128 + ((cc ^ (row & 7)) << 4));
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "r"(pack_bf16x2(__uint_as_float(o[i + 0]) * inv, __uint_as_float(o[i + 1]) * inv)),
-                                 "r"(pack_bf16x2(__uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv)),
-                                 "r"(pack_bf16x2(__uint_as_float(o[i + 4]) * inv, __uint_as_float(o[i + 5]) * inv)),
-                                 "r"(pack_bf16x2(__uint_as_float(o[i + 6]) * inv, __uint_as_float(o[i + 7]) * inv))
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float a, bb;
+                        fmul2(a, bb, __uint_as_float(o[i + 2 * j]), __uint_as_float(o[i + 2 * j + 1]), inv2);
+                        w4[j] = pack_bf16x2(a, bb);
+                    }
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w4[0]), "r"(w4[1]),
+                                 "r"(w4[2]), "r"(w4[3])
                                  : "memory");
                 }
             }
