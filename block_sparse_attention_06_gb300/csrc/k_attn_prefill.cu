@@ -24,10 +24,16 @@
 //   warp 1     TMEM owner and MMA issuer: S = Q K^T (M = 128, N = 128 tokens,
 //              K = D) into the S buffer of the tile's softmax group, then, once P
 //              is back in TMEM, O = P V with P as the TMEM A operand and V as an
-//              MN-major shared-memory B operand;
+//              MN-major shared-memory B operand.  Warps share a sub-partition's
+//              issue slots by warp index mod 4, and an MMA issuer that competes
+//              with busy warps feeds the tensor core at a fraction of its rate:
+//              sub-partition 1 holds only this warp, the store warp and one warp
+//              of each softmax group and of the epilogue (those must cover all
+//              four TMEM lane quarters), and each group of MMAs is issued from
+//              one asm block;
 //   warp 2     K/V loader: K_j by TMA (128B swizzle, 64-column boxes) once the
 //              previous chunk's last S has completed, V_j once its last PV has;
-//   warp 3     output store: the staged tile is one contiguous block of the
+//   warp 17    output store: the staged tile is one contiguous block of the
 //              CSR-ordered partials and leaves by TMA bulk tensor stores in a few
 //              power-of-two row boxes;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
@@ -39,7 +45,7 @@
 //              normalised, into the shared staging buffer in the 128B-swizzled
 //              box layout, so a softmax group goes on to its next tile as soon
 //              as its P is in TMEM;
-//   warps 16-18  Q loaders, one per Q buffer, one tile each in turn: the HPG
+//   warps 16, 3, 18  Q loaders, one per Q buffer, one tile each in turn: the HPG
 //              heads of each entry's query row (HPG * D * 2 contiguous bytes) by
 //              16-byte cp.async, in the 128B-swizzled layout the MMA reads.  One
 //              instruction moves 512 contiguous bytes, where a TMA box of the
@@ -136,6 +142,70 @@ __device__ __forceinline__ float sum2(uint64_t acc2) {
     float a, b;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(acc2));
     return a + b;
+}
+
+// KSTEPS MMAs of S = Q K^T (M = N = 128, K = 16 each), A and B K-major 128B-swizzled: the k-step
+// advances 32 bytes within a 64-column sub-tile and 16 KB between sub-tiles, i.e. +2 / +1024 in the
+// descriptors' 16-byte address units.  Issued by the threads with `leader` set (one thread).  The
+// first MMA overwrites D, the others accumulate.
+template <int KSTEPS>
+__device__ __forceinline__ void mma_s_block(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t leader) {
+    static_assert(KSTEPS == 4 || KSTEPS == 8, "D of 64 or 128");
+    if constexpr (KSTEPS == 8) {
+        asm volatile(
+            "{\n\t.reg .pred f, t, e;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+            "setp.ne.b32 e, %4, 0;\n\tsetp.ne.b32 f, %4, %4;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\tadd.s64 a4, %1, 1024;\n\t"
+            "add.s64 a5, %1, 1026;\n\tadd.s64 a6, %1, 1028;\n\tadd.s64 a7, %1, 1030;\n\t"
+            "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\tadd.s64 b4, %2, 1024;\n\t"
+            "add.s64 b5, %2, 1026;\n\tadd.s64 b6, %2, 1028;\n\tadd.s64 b7, %2, 1030;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, t;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(leader)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred f, t, e;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+            "setp.ne.b32 e, %4, 0;\n\tsetp.ne.b32 f, %4, %4;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+            "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(leader)
+            : "memory");
+    }
+}
+
+// Eight MMAs of O = P V (K = 16 tokens each): A = P in TMEM, 8 columns (16 bf16 pairs) per k-step;
+// B = V MN-major 128B-swizzled, 16 rows of 128 bytes per k-step (+128 descriptor units).  Issued by
+// the threads with `leader` set (one thread).  The first MMA overwrites D.
+__device__ __forceinline__ void mma_pv_block(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t leader) {
+    asm volatile(
+        "{\n\t.reg .pred f, t, e;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+        ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "setp.ne.b32 e, %4, 0;\n\tsetp.ne.b32 f, %4, %4;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\tadd.s32 a4, %1, 32;\n\t"
+        "add.s32 a5, %1, 40;\n\tadd.s32 a6, %1, 48;\n\tadd.s32 a7, %1, 56;\n\t"
+        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\tadd.s64 b4, %2, 512;\n\t"
+        "add.s64 b5, %2, 640;\n\tadd.s64 b6, %2, 768;\n\tadd.s64 b7, %2, 896;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(leader)
+        : "memory");
 }
 
 // Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
@@ -432,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (n_v > 0) mbar_wait(&sm.v_full, (n_v - 1) & 1, err, nullptr);
             }
         }
-    } else if (warp == 3) {
+    } else if (warp == 17) {
         // ------------------------------------------------------------ output store (lane 0)
         if (lane == 0) {
             for (int u = 0;; ++u) {
@@ -465,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             bulk_wait_all();
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer (lane 0)
+        // The warp shares its sub-partition with busy softmax and epilogue warps, and every issue
+        // slot it needs per MMA slows the tensor core down: each group of MMAs is one asm block.
         if (lane == 0) {
             int u = 0, cs_k = -1, cs_v = -1;
             bool have_prev = false;
@@ -481,10 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     if (!mbar_wait(&sm.v_full, cs_v & 1, err, &sm.abort)) return false;
                 }
                 tc_fence_after();
-                const uint32_t d_o = tmem + uint32_t(256 + b * D), a_p = tmem + uint32_t(b * 128);
-#pragma unroll
-                for (int kt = 0; kt < 8; ++kt)
-                    mma_bf16_ts(d_o, a_p + uint32_t(kt * 8), vd + uint64_t(kt * 2048 >> 4), kIdescO, kt > 0 ? 1u : 0u);
+                mma_pv_block(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128), vd, kIdescO, 1u);
                 mma_commit(&sm.o_full[b]);
                 if (flags & kFlagLast) mma_commit(&sm.v_empty);
                 return true;
@@ -503,14 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (!mbar_wait(&sm.q_full[qb], (u / kQBuf) & 1, err, &sm.abort)) break;
                 tc_fence_after();
                 const int b = u & 1;
-                const uint64_t qd = make_smem_desc(smem_u32(sm.q[qb]), 16, 1024, 2);
-                const uint32_t d_s = tmem + uint32_t(b * 128);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // the descriptor's start-address field counts 16-byte units
-                    const uint64_t o = uint64_t(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_bf16(d_s, qd + o, kd + o, kIdescS, kk > 0 ? 1u : 0u);
-                }
+                mma_s_block<D / 16>(tmem + uint32_t(b * 128), make_smem_desc(smem_u32(sm.q[qb]), 16, 1024, 2), kd,
+                                    kIdescS, 1u);
                 mma_commit(&sm.s_full[b]);
                 mma_commit(&sm.q_empty[qb]);
                 if (flags & kFlagLast) mma_commit(&sm.k_empty);
@@ -527,14 +590,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
-    } else if (warp >= 16) {
-        // ------------------------------------------------------------ Q loaders (warps 16-18)
+    } else if (warp == 3 || warp >= 16) {
+        // ------------------------------------------------------------ Q loaders (warps 16, 3, 18)
+        // (sub-partitions 0, 3 and 2: the MMA warp's sub-partition 1 keeps its issue slots)
         constexpr int CPH = D / 8;         // 16-byte chunks of one head row
         constexpr int CPE = HPG * CPH;     // of one entry (a multiple of 32)
         static_assert(CPE % 32 == 0, "an entry spans whole warps of 16-byte chunks");
         // this lane's chunks of an entry: head and chunk column of chunk j * 32 + lane
         const uint8_t *q_row0 = qg + size_t(lane % CPH) * 16;   // + head row offset below
-        const int qb = warp - 16;          // this warp's Q buffer: tiles u with u % kQBuf == qb
+        const int qb = warp == 16 ? 0 : warp == 3 ? 1 : 2;   // this warp's Q buffer: tiles u % kQBuf == qb
         for (int u = qb;; u += kQBuf) {
             const int slot = u % kRing;
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort))) break;
