@@ -27,15 +27,11 @@
 //              MN-major shared-memory B operand.  Warps share a sub-partition's
 //              issue slots by warp index mod 4, and an MMA issuer that competes
 //              with busy warps feeds the tensor core at a fraction of its rate:
-//              sub-partition 1 holds only this warp, the store warp and one warp
-//              of each softmax group and of the epilogue (those must cover all
-//              four TMEM lane quarters), and each group of MMAs is issued from
-//              one asm block;
+//              sub-partition 1 holds only this warp and one warp of each softmax
+//              group and of the epilogue (those must cover all four TMEM lane
+//              quarters), and each group of MMAs is issued from one asm block;
 //   warp 2     K/V loader: K_j by TMA (128B swizzle, 64-column boxes) once the
 //              previous chunk's last S has completed, V_j once its last PV has;
-//   warp 17    output store: the staged tile is one contiguous block of the
-//              CSR-ordered partials and leaves by TMA bulk tensor stores in a few
-//              power-of-two row boxes;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
 //              from TMEM in 32-column chunks twice (row max, then exp2 and P as
 //              packed bf16 written over S); the row's 1/sum goes to shared
@@ -44,7 +40,11 @@
 //   warps 12-15  epilogue: every tile in order, O chunk by chunk from TMEM,
 //              normalised, into the shared staging buffer in the 128B-swizzled
 //              box layout, so a softmax group goes on to its next tile as soon
-//              as its P is in TMEM;
+//              as its P is in TMEM.  A staged tile is one contiguous block of the
+//              CSR-ordered partials; each warp stages its own 32 rows and sends
+//              them by TMA bulk tensor stores in a few power-of-two row boxes, so
+//              no warp waits for another to reuse the staging buffer;
+//   warp 17    idle (it would share the MMA warp's sub-partition);
 //   warps 16, 3, 18  Q loaders, one per Q buffer, one tile each in turn: the HPG
 //              heads of each entry's query row (HPG * D * 2 contiguous bytes) by
 //              16-byte cp.async, in the 128B-swizzled layout the MMA reads.  One
@@ -94,7 +94,6 @@ struct AttnSmem {
     uint64_t q_full[kQBuf], q_empty[kQBuf];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
     uint64_t stat_free[2];                          // inv_le[b] read by the epilogue
-    uint64_t stg_full, stg_free;                    // staging buffer written / read by the store (one phase per tile)
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
     uint64_t drain;
@@ -315,12 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         }
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.v_empty, 1);
-        mbar_init(&sm.stg_full, 4);
-        mbar_init(&sm.stg_free, 1);
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.desc_ready[r], 32);
             mbar_init(&sm.desc_full[r], 1);   // the tile's Q loader, once it has read the descriptor
-            mbar_init(&sm.desc_empty[r], 10);   // MMA, store, a softmax group's 4 warps, the epilogue's 4
+            mbar_init(&sm.desc_empty[r], 9);   // MMA, a softmax group's 4 warps, the epilogue's 4
         }
         for (int r = 0; r < 4; ++r) {
             mbar_init(&sm.chunk_ready[r], 1);
@@ -460,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             for (int t = 0; t < nt; ++t) mbar_arrive(&sm.desc_ready[(u + t) % kRing]);
             u += nt;
         }
-        // end markers: three tiles (one per Q loader, and so one per softmax group; the MMA, store and
-        // epilogue warps stop at the first), one chunk
+        // end markers: three tiles (one per Q loader, and so one per softmax group; the MMA and epilogue
+        // warps stop at the first), one chunk
         for (int e = 0; ok && e < kQBuf; ++e) {
             const int slot = u % kRing;
             if (u >= kRing && !wait_lane0(&sm.desc_empty[slot], ((u / kRing) - 1) & 1)) break;
@@ -501,38 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (n_k > 0) mbar_wait(&sm.k_full, (n_k - 1) & 1, err, nullptr);
                 if (n_v > 0) mbar_wait(&sm.v_full, (n_v - 1) & 1, err, nullptr);
             }
-        }
-    } else if (warp == 17) {
-        // ------------------------------------------------------------ output store (lane 0)
-        if (lane == 0) {
-            for (int u = 0;; ++u) {
-                const int slot = u % kRing;
-                if (!mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort)) break;
-                const volatile TileDesc &d = sm.desc[slot];
-                const int flags = d.flags;
-                if (flags & kFlagEnd) break;
-                const int ent0 = d.ent0, n_valid = d.n_valid;
-                mbar_arrive(&sm.desc_empty[slot]);
-                if (!mbar_wait(&sm.stg_full, u & 1, err, &sm.abort)) break;
-                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 of the CSR-ordered partials, one
-                // contiguous block, in power-of-two boxes
-                int r0 = 0;
-                const int rows = n_valid * HPG;
-#pragma unroll
-                for (int b = 0; b < kStoreBoxes; ++b) {
-                    const int R = 128 >> b;
-                    if (rows & R) {
-#pragma unroll
-                        for (int i = 0; i < NSUB; ++i)
-                            tma_store_2d(&omaps.box[b], sm.stg + i * 16384 + r0 * 128, i * 64, ent0 * HPG + r0);
-                        r0 += R;
-                    }
-                }
-                bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(&sm.stg_free);
-            }
-            bulk_wait_all();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (lane 0)
@@ -590,7 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
-    } else if (warp == 3 || warp >= 16) {
+    } else if (warp == 17) {
+        // idle: this warp would take issue slots from the MMA warp's sub-partition
+    } else if (warp == 3 || warp == 16 || warp == 18) {
         // ------------------------------------------------------------ Q loaders (warps 16, 3, 18)
         // (sub-partitions 0, 3 and 2: the MMA warp's sub-partition 1 keeps its issue slots)
         constexpr int CPH = D / 8;         // 16-byte chunks of one head row
@@ -739,7 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         for (int u = 0;; ++u) {
             const int slot = u % kRing;
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort))) break;
-            const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
+            const volatile TileDesc &d = sm.desc[slot];
+            const int flags = d.flags;
+            const int ent0 = d.ent0, n_valid = d.n_valid;
             __syncwarp();
             if (flags & kFlagEnd) break;
             if (lane == 0) mbar_arrive(&sm.desc_empty[slot]);
@@ -751,8 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const uint64_t inv2 = dup2(sm.inv_le[b][row]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.stat_free[b]);
-            // the staging buffer is free once tile u - 1 has left it
-            if (u >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stg_free, (u - 1) & 1, err, &sm.abort))) break;
+            // this warp's 32 staging rows are free once its stores of tile u - 1 have read them
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -781,9 +751,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.o_free[b]);
-                mbar_arrive(&sm.stg_full);
+                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 of the CSR-ordered partials are one contiguous
+                // block; this warp's rows quad*32 .. quad*32+31 of it leave in power-of-two boxes (32, 16,
+                // 8, 4 rows; each starts on an 8-row, 1024-byte boundary of the swizzled staging layout)
+                const int rows = min(32, n_valid * HPG - quad * 32);
+                int r0 = quad * 32;
+#pragma unroll
+                for (int bx = 2; bx < kStoreBoxes; ++bx) {
+                    const int R = 128 >> bx;
+                    if (rows > 0 && (rows & R)) {
+#pragma unroll
+                        for (int i = 0; i < NSUB; ++i)
+                            tma_store_2d(&omaps.box[bx], sm.stg + i * 16384 + r0 * 128, i * 64, ent0 * HPG + r0);
+                        r0 += R;
+                    }
+                }
+                bulk_commit();
             }
         }
+        if (lane == 0) bulk_wait_all();   // the partials are written before the CTA exits
     }
 
     tc_fence_before();
