@@ -6,14 +6,19 @@
 // 架构/特性 and 解码索引评分内核优化: one score per 128-token block and KV group).
 //
 // One CTA owns (KV group g, 128 consecutive query rows, a chunk of up to 128
-// blocks).  Warp roles:
+// blocks).  The rows may belong to several requests (a ragged multi-request
+// chunk): the CTA then scores the tile once per request it holds, against that
+// request's pages, and keeps each row's scores from its own request's pass.
+// Warp roles:
 //   warp 0     TMA producer: the q_idx tile once, then one k-index page per block
 //              into a 4-stage ring (128B / 64B swizzle);
 //   warp 1     TMEM owner and MMA issuer: tcgen05.mma kind::f16, M = 128 rows,
 //              N = 128 tokens, K = Di, into one of two TMEM accumulators;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = row), masked max
 //              over the 128 token columns, 32 blocks staged in shared memory and
-//              written out as coalesced 128-byte row segments.
+//              written out by each warp for its own 32 rows as coalesced 128-byte
+//              row segments (no barrier across warps, so a timeout cannot leave a
+//              warp waiting for another).
 // All waits are bounded; a timeout raises MSA_FLAG_TIMEOUT and drains.
 #include "msa_device.cuh"
 #include "msa_internal.h"
@@ -37,12 +42,13 @@ struct ScoreSmem {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    int jmax;
-    int req;
-    int mixed;
+    int n_pass;                 // distinct requests among the tile's rows
+    int pass_req[128];          // request of each pass, in order of first appearance
+    int pass_j1[128];           // one past the last candidate block of the pass's rows (chunk-clipped later)
+    int row_req[128];           // request of each tile row, -1 past n_rows or for an invalid row
+    int row_pass[128];          // pass index of each valid row
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
@@ -64,47 +70,92 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j0 = chunk * kChunk;
 
-    if (tid == 0) {
-        sm.jmax = -1;
-        sm.mixed = 0;
-        sm.abort = 0;
-        sm.req = q_req[row0];
-    }
-    __syncthreads();
-    if (tid < 128 && row0 + tid < n_rows) {
-        const int p = q_pos[row0 + tid];
-        const int rq = q_req[row0 + tid];
-        if (rq != sm.req) sm.mixed = 1;
-        if (p < 0 || (p >> 7) >= max_blocks) {
-            sm.mixed = 2;
-        } else {
-            atomicMax(&sm.jmax, p >> 7);
+    int row_jmax = -1;          // (thread < 128) own block of the thread's row
+    int rq = -1;                // (thread < 128) request of the thread's row, -1 if none / invalid
+    const int rq0 = q_req[min(row0, n_rows - 1)];
+    if (tid == 0) sm.abort = 0;
+    if (tid < 128) {
+        const int grow = row0 + tid;
+        if (grow < n_rows) {
+            const int p = q_pos[grow];
+            rq = q_req[grow];
+            if (rq < 0 || rq >= n_req || p < 0 || (p >> 7) >= max_blocks) {
+                if (chunk == 0 && g == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+                rq = -1;
+            } else {
+                row_jmax = p >> 7;
+            }
         }
+        sm.row_req[tid] = rq;
+        sm.pass_j1[tid] = -1;
+    }
+    // the common case: every valid row of the tile belongs to the first row's request
+    const bool one_req =
+        __syncthreads_and(tid >= 128 || rq < 0 || rq == rq0) && rq0 >= 0 && rq0 < n_req;
+    if (one_req) {
+        if (tid == 0) {
+            sm.pass_req[0] = rq0;
+            sm.n_pass = 1;
+        }
+        if (tid < 128 && rq >= 0) atomicMax(&sm.pass_j1[0], row_jmax + 1);
+    } else {
+        if (tid == 0) {
+            // distinct requests in order of first appearance; a run of equal requests costs one compare
+            int n = 0, prev = -1, prev_k = -1;
+            for (int i = 0; i < 128; ++i) {
+                const int r = sm.row_req[i];
+                int k = -1;
+                if (r >= 0) {
+                    if (r == prev) {
+                        k = prev_k;
+                    } else {
+                        k = 0;
+                        while (k < n && sm.pass_req[k] != r) ++k;
+                        if (k == n) sm.pass_req[n++] = r;
+                    }
+                    prev = r;
+                    prev_k = k;
+                }
+                sm.row_pass[i] = k;
+            }
+            sm.n_pass = n;
+        }
+        __syncthreads();
+        if (tid < 128 && sm.row_pass[tid] >= 0) atomicMax(&sm.pass_j1[sm.row_pass[tid]], row_jmax + 1);
     }
     __syncthreads();
-    const int req = sm.req;
-    if (sm.mixed || req < 0 || req >= n_req) {
-        if (tid == 0 && chunk == 0 && g == 0)
-            raise_flag(err, sm.mixed == 1 ? MSA_FLAG_UNSUPPORTED : MSA_FLAG_BOUNDS);
-        return;
-    }
+    const int n_pass = sm.n_pass;
     const int j_end_chunk = min(j0 + kChunk, max_blocks);
-    const int j1 = min(j_end_chunk, sm.jmax + 1);       // blocks [j0, j1) hold candidates
-    const int nblk = j1 - j0;
+    // blocks [j0, pass_end(k)) hold candidates of pass k's rows
+    auto pass_end = [&](int k) { return min(j_end_chunk, max(j0, sm.pass_j1[k])); };
+    int total = 0;
+    for (int k = 0; k < n_pass; ++k) total += pass_end(k) - j0;
 
-    // rows of this tile; blocks past every row's own block are -inf
-    auto fill_neg_inf = [&](int from, int to) {
-        if (from >= to || tid < 64) return;
+    // blocks past a row's request's candidates are -inf (all of the chunk for a row without a valid
+    // request; with a single request, the scores of an invalid row are left as they are)
+    auto fill_neg_inf = [&]() {
+        if (tid < 64) return;
         const int e = tid - 64;                          // 128 epilogue threads
+        if (one_req) {
+            const int from = pass_end(0);
+            if (from >= j_end_chunk) return;
+            for (int i = 0; i < 128 && row0 + i < n_rows; ++i) {
+                float *o = scores + (size_t(row0 + i) * G + g) * max_blocks;
+                for (int j = from + e; j < j_end_chunk; j += 128) o[j] = -INFINITY;
+            }
+            return;
+        }
         for (int i = 0; i < 128; ++i) {
             const int grow = row0 + i;
             if (grow >= n_rows) break;
+            const int k = sm.row_pass[i];
+            const int from = k >= 0 ? pass_end(k) : j0;
             float *o = scores + (size_t(grow) * G + g) * max_blocks;
-            for (int j = from + e; j < to; j += 128) o[j] = -INFINITY;
+            for (int j = from + e; j < j_end_chunk; j += 128) o[j] = -INFINITY;
         }
     };
-    if (nblk <= 0) {
-        fill_neg_inf(j0, j_end_chunk);
+    if (total <= 0) {
+        fill_neg_inf();
         return;
     }
 
@@ -136,18 +187,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             tma_prefetch_desc(&bmap);
             mbar_arrive_expect_tx(&sm.a_full, Smem::kTileBytes);
             tma_load_3d(sm.a, &amap, &sm.a_full, 0, g, row0);
-            int issued = 0;
-            for (int jj = 0; jj < nblk; ++jj) {
-                const int s = jj % kStages;
-                if (jj >= kStages && !mbar_wait(&sm.empty[s], ((jj / kStages) - 1) & 1, err, &sm.abort)) break;
-                int page = block_table[size_t(req) * max_blocks + j0 + jj];
-                if (page < 0 || page >= n_pages) {
-                    raise_flag(err, MSA_FLAG_BOUNDS);
-                    page = 0;
+            int issued = 0, it = 0;          // blocks over all passes
+            bool ok = true;
+            for (int pk = 0; ok && pk < n_pass; ++pk) {
+                const int req = sm.pass_req[pk], nb = pass_end(pk) - j0;
+                for (int jj = 0; jj < nb; ++jj, ++it) {
+                    const int s = it % kStages;
+                    if (it >= kStages && !mbar_wait(&sm.empty[s], ((it / kStages) - 1) & 1, err, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    int page = block_table[size_t(req) * max_blocks + j0 + jj];
+                    if (page < 0 || page >= n_pages) {
+                        raise_flag(err, MSA_FLAG_BOUNDS);
+                        page = 0;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[s], Smem::kTileBytes);
+                    tma_load_4d(sm.b[s], &bmap, &sm.full[s], 0, g, 0, page);
+                    issued = it + 1;
                 }
-                mbar_arrive_expect_tx(&sm.full[s], Smem::kTileBytes);
-                tma_load_4d(sm.b[s], &bmap, &sm.full[s], 0, g, 0, page);
-                issued = jj + 1;
             }
             // on abort: let every issued copy land before the CTA can exit
             if (sm.abort) {
@@ -160,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
         if (lane == 0) {
             const uint32_t a_addr = smem_u32(sm.a);
             bool ok = mbar_wait(&sm.a_full, 0, err, &sm.abort);
-            for (int jj = 0; ok && jj < nblk; ++jj) {
+            for (int jj = 0; ok && jj < total; ++jj) {   // blocks over all passes
                 const int s = jj % kStages;
                 const int acc = jj & 1;
                 if (!mbar_wait(&sm.full[s], (jj / kStages) & 1, err, &sm.abort)) break;
@@ -186,12 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
         const int row = quad * 32 + lane;
         const int grow = row0 + row;
         const int p = grow < n_rows ? q_pos[grow] : -1;
-        const int ew = warp - 2;
         const uint32_t lane_addr = tmem + (uint32_t(quad * 32) << 16);
-        int jj = 0;
-        for (; jj < nblk; ++jj) {
-            const int acc = jj & 1;
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full[acc], (jj >> 1) & 1, err, &sm.abort));
+        bool ok = true;
+        int it = 0;                                      // blocks over all passes
+        for (int pk = 0; ok && pk < n_pass; ++pk) {
+        const int req = sm.pass_req[pk], nblk = pass_end(pk) - j0;
+        for (int jj = 0; jj < nblk; ++jj, ++it) {
+            const int acc = it & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full[acc], (it >> 1) & 1, err, &sm.abort));
             if (!ok) break;
             tc_fence_after();
             const int lim = p - (j0 + jj) * 128;     // columns c <= lim are visible
@@ -215,24 +275,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
             sm.sc[row][jj & 31] = best;
             if ((jj & 31) == 31 || jj == nblk - 1) {
-                epi_bar();
+                // the warp writes back its own 32 rows, one coalesced 128-byte segment per row
+                __syncwarp();
                 const int base = jj & ~31;
                 const int ncols = jj - base + 1;
                 for (int i = 0; i < 32; ++i) {
-                    const int r = ew * 32 + i;
+                    const int r = quad * 32 + i;
                     const int gr = row0 + r;
-                    if (gr < n_rows && lane < ncols)
+                    if (gr < n_rows && lane < ncols && (one_req || sm.row_req[r] == req))   // this pass's rows
                         scores[(size_t(gr) * G + g) * max_blocks + j0 + base + lane] = sm.sc[r][lane];
                 }
-                epi_bar();
+                __syncwarp();
             }
+        }
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    fill_neg_inf(j1, j_end_chunk);
+    fill_neg_inf();
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
 

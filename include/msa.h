@@ -102,9 +102,12 @@ typedef void *msa_stream_t;
  *   scores      fp32 [n_rows][G][max_blocks]  out; -inf for blocks > q_pos/128
  *   phase       MSA_PHASE_DECODE: each row streams its own candidate pages
  *               (HBM-bound path, any rows).  MSA_PHASE_PREFILL: rows are
- *               scored 128 at a time on the tensor cores; every run of 128
- *               consecutive rows (the last may be shorter) must belong to one
- *               request, otherwise MSA_FLAG_UNSUPPORTED is raised.
+ *               scored 128 at a time on the tensor cores.  The rows of a chunk
+ *               may belong to several requests (a ragged multi-request chunked
+ *               prefill): a run of 128 consecutive rows that holds rows of m
+ *               requests is scored m times, once against each request's pages,
+ *               so this phase suits chunks of a few long requests; single-token
+ *               (decode) rows belong on MSA_PHASE_DECODE.
  * A page id outside [0, n_pages) or a q_pos/128 >= max_blocks raises
  * MSA_FLAG_BOUNDS.
  */

@@ -226,6 +226,42 @@ def prefill_case(prefix: int, chunk: int, Hq: int, G: int, D: int, Di: int, topk
                 torch.zeros(chunk, dtype=torch.int32, device=device), pos, max_blocks, [], name)
 
 
+def ragged_prefill_case(prefixes: Sequence[int], chunks: Sequence[int], Hq: int, G: int, D: int,
+                        Di: int, topk: int, pool_pages: int, seed: int, device="cpu", span: int = 256,
+                        span_sigma: float = 0.5, name: str = "") -> Case:
+    """One prefill chunk holding several requests, as a chunked-prefill engine
+    batches them: request r contributes chunks[r] new rows at positions
+    prefixes[r] .. prefixes[r]+chunks[r]-1 over a cache of prefixes[r]+chunks[r]
+    tokens.  The rows are concatenated in request order, so 128-row tiles may
+    straddle requests.  Per request, the query-side index vectors follow the same
+    span structure as prefill_case."""
+    assert len(prefixes) == len(chunks) and len(chunks) > 0
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    lens = [p + c for p, c in zip(prefixes, chunks)]
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages(lens, pool_pages, page, gc)
+    gd = _gen(seed + 7919, device)
+    n_rows = sum(chunks)
+    q = _randn_f32((n_rows, Hq, D), gd, device).to(torch.bfloat16)
+    parts_idx, parts_req, parts_pos = [], [], []
+    for r, (p, c) in enumerate(zip(prefixes, chunks)):
+        n_span = (c + span - 1) // span
+        centres = _randn_f32((n_span, G, Di), gd, device)
+        noise = _randn_f32((c, G, Di), gd, device)
+        span_of_row = torch.arange(c, device=device) // span
+        parts_idx.append(centres[span_of_row] + span_sigma * noise)
+        parts_req.append(torch.full((c,), r, dtype=torch.int32, device=device))
+        parts_pos.append(torch.arange(p, p + c, dtype=torch.int32, device=device))
+    q_idx = torch.cat(parts_idx).to(torch.bfloat16)
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    return Case(dims, k_cache, v_cache, kidx, bt.to(device),
+                torch.tensor(lens, dtype=torch.int32, device=device), q, q_idx,
+                torch.cat(parts_req), torch.cat(parts_pos), max_blocks, [], name)
+
+
 def tiny_case(seed: int = 1000, device="cpu", L: int = 2048, n_decode: int = 16,
               Hq: int = 8, G: int = 2, D: int = 64, Di: int = 32, topk: int = 4,
               pool_pages: int = 32, needles_per_group: int = 2) -> Tuple[Case, Case]:

@@ -75,6 +75,19 @@ def test_small_prefill_ragged(msa, prefix, chunk):
     _check_prefill(msa, case)
 
 
+@pytest.mark.parametrize("prefixes,chunks,hq,g,d,di", [
+    ([300, 0, 1000], [100, 257, 129], 16, 2, 128, 64),     # 128-row tiles straddle two requests
+    ([0, 5000, 64, 130], [1, 300, 63, 200], 8, 2, 64, 32),  # a one-row request, several per tile
+    ([2000, 2000], [384, 128], 32, 8, 128, 64),             # tile-aligned requests
+])
+def test_prefill_ragged_multi_request(msa, prefixes, chunks, hq, g, d, di):
+    """One chunk holding several requests back to back (chunked prefill of a batch): every
+    step of the prefill path against the oracle on all rows."""
+    case = mi.ragged_prefill_case(prefixes, chunks, Hq=hq, G=g, D=d, Di=di, topk=6, pool_pages=120,
+                                  seed=21, device=DEV)
+    _check_prefill(msa, case)
+
+
 @pytest.mark.parametrize("hq,g,d,di", [(32, 8, 128, 64), (16, 4, 64, 32), (8, 2, 128, 32)])
 def test_prefill_shape_variants(msa, hq, g, d, di):
     case = mi.prefill_case(2100, 400, Hq=hq, G=g, D=d, Di=di, topk=8, pool_pages=40, seed=13, device=DEV)
