@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libmsa.so")
 
 MSA_PHASE_DECODE = 0
 MSA_PHASE_PREFILL = 1
+MSA_PHASE_DECODE_MULTI = 2
 MSA_OP_INVERT = 0
 MSA_OP_DECODE = 1
 MSA_OP_PREFILL = 2

@@ -151,6 +151,9 @@ msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const in
     else if (phase == MSA_PHASE_PREFILL)
         e = launch_score_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores,
                                  err_word, cs);
+    else if (phase == MSA_PHASE_DECODE_MULTI)
+        e = launch_score_decode_mt(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores,
+                                   err_word, cs);
     else
         return fail(MSA_ERR_INVALID_ARG, "msa_index_score: unknown phase %d", phase);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_score");

@@ -40,6 +40,10 @@ cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32
                                 int n_pages, const Shape &s, float *scores, int32_t *err,
                                 cudaStream_t st);
 
+// Multi-token decode scoring: rows grouped by request (q_req non-decreasing, <= 16 rows each).
+cudaError_t launch_score_decode_mt(const void *q_idx, const void *kidx, const int32_t *block_table,
+                                   const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req, int n_pages,
+                                   const Shape &s, float *scores, int32_t *err, cudaStream_t st);
 cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int32_t *block_table,
                                  const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
                                  int n_pages, const Shape &s, float *scores, int32_t *err,

@@ -80,8 +80,9 @@ typedef struct {
 typedef void *msa_stream_t;
 
 /* Phase selector of msa_index_score. */
-#define MSA_PHASE_DECODE  0
-#define MSA_PHASE_PREFILL 1
+#define MSA_PHASE_DECODE       0
+#define MSA_PHASE_PREFILL      1
+#define MSA_PHASE_DECODE_MULTI 2
 
 /* Operation selector of msa_workspace_bytes. */
 #define MSA_OP_INVERT  0
@@ -108,6 +109,13 @@ typedef void *msa_stream_t;
  *               requests is scored m times, once against each request's pages,
  *               so this phase suits chunks of a few long requests; single-token
  *               (decode) rows belong on MSA_PHASE_DECODE.
+ *               MSA_PHASE_DECODE_MULTI: several decode rows per request
+ *               (speculative or multi-token decode) share one read of each
+ *               candidate page: keys as the M side of bf16 tensor-core MMAs, the
+ *               request's rows as N ([T-zh 解码索引评分内核优化], the AB-swapped
+ *               formulation).  Rows must be grouped by request (q_req
+ *               non-decreasing, else MSA_FLAG_UNSUPPORTED) with at most 16 rows
+ *               per request (else MSA_FLAG_UNSUPPORTED); max_blocks <= 65535.
  * A page id outside [0, n_pages) or a q_pos/128 >= max_blocks raises
  * MSA_FLAG_BOUNDS.
  */

@@ -226,6 +226,30 @@ def prefill_case(prefix: int, chunk: int, Hq: int, G: int, D: int, Di: int, topk
                 torch.zeros(chunk, dtype=torch.int32, device=device), pos, max_blocks, [], name)
 
 
+def multi_token_decode_case(lens: Sequence[int], T: int, Hq: int, G: int, D: int, Di: int, topk: int,
+                            pool_pages: int, seed: int, device="cpu", name: str = "") -> Case:
+    """Multi-token (speculative) decode: request b holds lens[b] cached tokens, the
+    last T of them new; its T query rows sit at positions lens[b]-T .. lens[b]-1 and
+    are consecutive rows, requests in order (rows grouped by request)."""
+    assert T >= 1 and all(L >= T for L in lens)
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages(list(lens), pool_pages, page, gc)
+    gd = _gen(seed + 7919, device)
+    n_rows = T * len(lens)
+    q = _randn_f32((n_rows, Hq, D), gd, device).to(torch.bfloat16)
+    q_idx = _randn_f32((n_rows, G, Di), gd, device).to(torch.bfloat16)
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    q_req = torch.arange(len(lens), dtype=torch.int32, device=device).repeat_interleave(T)
+    q_pos = torch.cat([torch.arange(L - T, L, dtype=torch.int32, device=device) for L in lens])
+    return Case(dims, k_cache, v_cache, kidx, bt.to(device),
+                torch.tensor(list(lens), dtype=torch.int32, device=device), q, q_idx, q_req, q_pos, max_blocks, [],
+                name)
+
+
 def ragged_prefill_case(prefixes: Sequence[int], chunks: Sequence[int], Hq: int, G: int, D: int,
                         Di: int, topk: int, pool_pages: int, seed: int, device="cpu", span: int = 256,
                         span_sigma: float = 0.5, name: str = "") -> Case:
