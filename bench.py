@@ -188,6 +188,7 @@ def run_msa(args, rank, world, local):
     if args.only in ("all", "decode"):
         dec, case = bench_decode(args, rank, world, local, dev, peaks, peak_src)
         line.update(dec)
+        line["decode_multi"] = bench_decode_multi(args, world, dev, peaks, peak_src)
     if args.only in ("all", "prefill"):
         line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src)
     line["clocks"] = clocks.stop()
@@ -294,6 +295,53 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / K},
     }, case
+
+
+def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
+    """Multi-token (speculative) decode scoring: decode60k's 8 requests with T query rows each.  The
+    MSA_PHASE_DECODE_MULTI scan reads each request's k-index once for all its rows; the row-wise scan
+    (MSA_PHASE_DECODE) on the same rows reads it T times.  Reported: scored rows per second of the
+    multi-token scan and its HBM roofline against the k-index bytes read once per request."""
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+    K, W = args.steps, args.warmup
+    case = mi.multi_token_decode_case([60000] * 8, T, Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=4096,
+                                      seed=1001, device=dev)
+    dims = msa.dims_of(case)
+    err = msa.new_err_word(dev)
+    sc = torch.empty((case.n_rows, dims.G, dims.max_blocks), dtype=torch.float32, device=dev)
+
+    def timed(phase):
+        f = lambda: msa.msa_index_score(case.q_idx, case.kidx_cache, case.block_table, case.q_req, case.q_pos,
+                                        dims, phase, scores=sc, err_word=err)
+        for _ in range(W):
+            f()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        msa.msa_check(err)
+        return max_over_ranks(a.elapsed_time(b), world, dev) / K
+
+    multi_ms = timed(msa.MSA_PHASE_DECODE_MULTI)
+    row_ms = timed(msa.MSA_PHASE_DECODE)
+    kbytes = sum(int(L) for L in case.seq_lens.tolist()) * dims.G * dims.Di * 2
+    gbs = kbytes / (multi_ms / 1e3) / 1e9
+    return {
+        "metric": "multi-token decode scoring rows/s", "value": aggregate_throughput(case.n_rows, world, multi_ms / 1e3),
+        "unit": "rows/s", "ms_per_launch": multi_ms, "rowwise_ms_per_launch": row_ms,
+        "config": {"workload": f"decode60k with {T} query rows per request", "batch": 8, "rows": case.n_rows,
+                   "ctx": 60000, "G": dims.G, "Di": dims.Di},
+        "roofline": {"bound": "hbm", "kernel": "k_score_decode_mt", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": kbytes,
+                     "peak_source": f"{peak_src} hbm_gbs"},
+    }
 
 
 def bench_prefill(args, world, dev, peaks, peak_src):

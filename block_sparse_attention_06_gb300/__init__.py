@@ -75,6 +75,7 @@ def _load() -> ctypes.CDLL:
         "msa_lse_merge": [P, P, P, P, I, D, P, P, P, P],
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
         "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
+        "msa_offload_gather": [P, P, I, P, I, D, P, P, P, P, P],
         "msa_check": [P, P],
     }
     for name, argt in sigs.items():
@@ -316,6 +317,40 @@ def msa_sparse_attn_decode(q, k_cache, v_cache, page_table, row_len, dims: Dims,
     return out, lse
 
 
+def msa_offload_gather(host_k_cache, host_v_cache, page_table, dims: Dims, pool_k=None, pool_v=None,
+                       pool_page_table=None, err_word=None):
+    """Gather the selected group slices of host-resident K/V pages into a device pool;
+    returns (pool_k, pool_v, pool_page_table) for msa_sparse_attn_decode."""
+    for t, name in ((host_k_cache, "host_k_cache"), (host_v_cache, "host_v_cache")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous bf16 CPU tensor")
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be page-locked (pin_memory)")
+        if t.dim() != 4 or tuple(t.shape[1:]) != (dims.page_size, dims.G, dims.D):
+            raise ValueError(f"{name} must be [n_pages][128][G][D]")
+    if tuple(host_v_cache.shape) != tuple(host_k_cache.shape):
+        raise ValueError("host_v_cache must match host_k_cache")
+    rows = page_table.shape[0]
+    _req(page_table, torch.int32, "page_table", (rows, dims.topk))
+    if rows % dims.G:
+        raise ValueError("page_table rows must be B*G")
+    B = rows // dims.G
+    dev = page_table.device
+    shape = (B * dims.topk, dims.page_size, dims.G, dims.D)
+    pool_k = torch.empty(shape, dtype=torch.bfloat16, device=dev) if pool_k is None else pool_k
+    pool_v = torch.empty(shape, dtype=torch.bfloat16, device=dev) if pool_v is None else pool_v
+    _req(pool_k, torch.bfloat16, "pool_k", shape)
+    _req(pool_v, torch.bfloat16, "pool_v", shape)
+    if pool_page_table is None:
+        pool_page_table = torch.empty_like(page_table)
+    _req(pool_page_table, torch.int32, "pool_page_table", tuple(page_table.shape))
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_offload_gather", _ptr(host_k_cache), _ptr(host_v_cache), host_k_cache.shape[0], _ptr(page_table), B,
+          ctypes.byref(d), _ptr(pool_k), _ptr(pool_v), _ptr(pool_page_table), _ptr(err_word), _stream(dev))
+    return pool_k, pool_v, pool_page_table
+
+
 def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, dims: Dims, scores=None,
                     sel=None, page_table=None, row_len=None, out=None, lse=None, workspace=None, err_word=None):
     """One whole decode step (index scan, top-k, page tables, sparse attention) in one
@@ -402,6 +437,22 @@ class DecodeStep:
     def composed(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos):
         self.scores_only(q_idx, kidx_cache, block_table, q_pos)
         return self.rest(q, k_cache, v_cache, block_table, q_pos, seq_lens)
+
+    def offloaded(self, q, q_idx, host_k_cache, host_v_cache, kidx_cache, block_table, seq_lens, q_pos):
+        """The step with K/V in page-locked host memory and the k-index on the GPU: scan,
+        top-k and page tables on the GPU, then only the selected pages are gathered into a
+        device pool (msa_offload_gather) and attended there."""
+        self.scores_only(q_idx, kidx_cache, block_table, q_pos)
+        msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
+        msa_build_page_table(self.sel, block_table, seq_lens, self.n_pages, self.dims, self.page_table,
+                             self.row_len, err_word=self.err)
+        if getattr(self, "_pool", None) is None:
+            self._pool = (None, None, None)
+        pk, pv, ppt = msa_offload_gather(host_k_cache, host_v_cache, self.page_table, self.dims, *self._pool,
+                                         err_word=self.err)
+        self._pool = (pk, pv, ppt)
+        return msa_sparse_attn_decode(q, pk, pv, ppt, self.row_len, self.dims, self.out, self.lse, self.workspace,
+                                      err_word=self.err)
 
     def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos=None):
         msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, self.dims, self.scores,

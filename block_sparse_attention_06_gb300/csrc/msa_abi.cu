@@ -276,6 +276,31 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_attn_decode");
 }
 
+msa_status_t msa_offload_gather(const void *host_k_cache, const void *host_v_cache, int32_t n_host_pages,
+                                const int32_t *page_table, int32_t B, const msa_dims_t *dims, void *pool_k,
+                                void *pool_v, int32_t *pool_page_table, int32_t *err_word, msa_stream_t stream) {
+    Shape s;
+    msa_status_t st = check_dims(dims, true, false, &s, "msa_offload_gather");
+    if (st != MSA_OK) return st;
+    MSA_REQUIRE(B >= 0 && n_host_pages > 0, "msa_offload_gather: bad sizes");
+    if (B == 0) return MSA_OK;
+    MSA_REQUIRE(host_k_cache && host_v_cache && page_table && pool_k && pool_v && pool_page_table && err_word,
+                "msa_offload_gather: NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(host_k_cache) | reinterpret_cast<uintptr_t>(host_v_cache) |
+         reinterpret_cast<uintptr_t>(pool_k) | reinterpret_cast<uintptr_t>(pool_v)) & 15u)
+        return fail(MSA_ERR_INVALID_ARG, "msa_offload_gather: caches and pools must be 16-byte aligned");
+    // the GPU reads the host caches in place: they must be page-locked and mapped
+    void *dk = nullptr, *dv = nullptr;
+    if (cudaHostGetDevicePointer(&dk, const_cast<void *>(host_k_cache), 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&dv, const_cast<void *>(host_v_cache), 0) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MSA_ERR_INVALID_ARG, "msa_offload_gather: host caches must be page-locked host memory");
+    }
+    cudaError_t e = launch_offload_gather(dk, dv, page_table, B, n_host_pages, s, pool_k, pool_v, pool_page_table,
+                                          err_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_offload_gather");
+}
+
 msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cache, const void *v_cache,
                              const void *kidx_cache, const int32_t *block_table, const int32_t *seq_lens, int32_t B,
                              int32_t n_pages, const msa_dims_t *dims, float *scores, int32_t *sel,

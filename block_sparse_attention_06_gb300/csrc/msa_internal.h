@@ -40,6 +40,10 @@ cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32
                                 int n_pages, const Shape &s, float *scores, int32_t *err,
                                 cudaStream_t st);
 
+// Selected K/V pages from host memory into a device pool (zero-copy gather).
+cudaError_t launch_offload_gather(const void *host_k, const void *host_v, const int32_t *page_table, int B,
+                                  int n_host_pages, const Shape &s, void *pool_k, void *pool_v,
+                                  int32_t *pool_page_table, int32_t *err, cudaStream_t st);
 // Multi-token decode scoring: rows grouped by request (q_req non-decreasing, <= 16 rows each).
 cudaError_t launch_score_decode_mt(const void *q_idx, const void *kidx, const int32_t *block_table,
                                    const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req, int n_pages,

@@ -252,6 +252,31 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
                                     msa_stream_t stream);
 
 /*
+ * msa_offload_gather -- K/V offload with the k-index kept on the GPU.  [T-zh 未来工作]:
+ * the KV cache may sit in host memory while the k-index stays resident; only the
+ * pages the selection picked are fetched.  The GPU reads the page-locked host
+ * caches in place (zero copy over the host link) and writes each selected group
+ * slice into a device pool, so msa_sparse_attn_decode runs on the pool unchanged.
+ *
+ *   host_k_cache, host_v_cache  bf16 [n_host_pages][128][G][D], page-locked host
+ *                    memory (cudaHostAlloc / cudaHostRegister), 16-byte aligned;
+ *                    caller-owned, only read
+ *   page_table       int32 [B*G][topk] device, host page ids (msa_build_page_table
+ *                    on the host block table), -1 padding
+ *   pool_k, pool_v   bf16 [B*topk][128][G][D] device, out: pool page b*topk + s
+ *                    holds, in group slice g, the slice g of host page
+ *                    page_table[b*G + g][s]
+ *   pool_page_table  int32 [B*G][topk] device, out: the pool page of each slot (-1
+ *                    where page_table is -1); pass it with the pools and
+ *                    n_pages = B*topk to msa_sparse_attn_decode
+ * A host page id >= n_host_pages raises MSA_FLAG_BOUNDS and its slot is not
+ * copied.  Host caches that are not page-locked give MSA_ERR_INVALID_ARG.
+ */
+msa_status_t msa_offload_gather(const void *host_k_cache, const void *host_v_cache, int32_t n_host_pages,
+                                const int32_t *page_table, int32_t B, const msa_dims_t *dims, void *pool_k,
+                                void *pool_v, int32_t *pool_page_table, int32_t *err_word, msa_stream_t stream);
+
+/*
  * msa_decode_step -- one whole decode step for B requests, each with one new
  * query token at position seq_lens[b] - 1: index scan (msa_index_score,
  * MSA_PHASE_DECODE, rows = requests), top-k (msa_topk_blocks), page tables
