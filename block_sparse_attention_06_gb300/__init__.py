@@ -26,6 +26,7 @@ MSA_PHASE_DECODE_MULTI = 2
 MSA_OP_INVERT = 0
 MSA_OP_DECODE = 1
 MSA_OP_PREFILL = 2
+MSA_OP_SELECT_PREFILL = 3
 
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
           4: "MSA_ERR_DEVICE_BOUNDS", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_WORKSPACE",
@@ -76,6 +77,7 @@ def _load() -> ctypes.CDLL:
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
         "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
         "msa_offload_gather": [P, P, I, P, I, D, P, P, P, P, P],
+        "msa_select_prefill": [P, P, P, P, P, I, I, I, D, P, P, S, P, P],
         "msa_check": [P, P],
     }
     for name, argt in sigs.items():
@@ -165,6 +167,37 @@ def msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, dims: Dims, ph
           n_rows, block_table.shape[0], kidx_cache.shape[0], ctypes.byref(d), phase, _ptr(scores),
           _ptr(err_word), _stream(dev))
     return scores
+
+
+def msa_select_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, dims: Dims, sel=None, workspace=None,
+                       err_word=None):
+    """Prefill scoring and top-k in one pass (the selection of msa_index_score +
+    msa_topk_blocks, without the scores); topk <= 16."""
+    n_rows = q_idx.shape[0]
+    _req(q_idx, torch.bfloat16, "q_idx", (n_rows, dims.G, dims.Di))
+    _req(kidx_cache, torch.bfloat16, "kidx_cache")
+    if kidx_cache.dim() != 4 or tuple(kidx_cache.shape[1:]) != (dims.page_size, dims.G, dims.Di):
+        raise ValueError("kidx_cache must be [n_pages][128][G][Di]")
+    _req(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or block_table.shape[1] != dims.max_blocks:
+        raise ValueError("block_table must be [n_req][max_blocks]")
+    _req(q_req, torch.int32, "q_req", (n_rows,))
+    _req(q_pos, torch.int32, "q_pos", (n_rows,))
+    dev = q_idx.device
+    n_req = block_table.shape[0]
+    if sel is None:
+        sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, device=dev)
+    _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    need = msa_workspace_bytes(MSA_OP_SELECT_PREFILL, n_rows, n_req, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    _req(workspace, torch.uint8, "workspace")
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_select_prefill", _ptr(q_idx), _ptr(kidx_cache), _ptr(block_table), _ptr(q_req), _ptr(q_pos), n_rows,
+          n_req, kidx_cache.shape[0], ctypes.byref(d), _ptr(sel), _ptr(workspace), workspace.numel(), _ptr(err_word),
+          _stream(dev))
+    return sel
 
 
 def msa_topk_blocks(scores, q_pos, dims: Dims, sel=None, err_word=None):
@@ -462,12 +495,25 @@ class DecodeStep:
 
 class PrefillStep:
     """One MSA prefill chunk: tensor-core index scoring -> top-k -> {q,blk}->{blk,q}
-    inversion -> KV-block-major sparse attention -> LSE merge."""
+    inversion -> KV-block-major sparse attention -> LSE merge.
 
-    def __init__(self, dims: Dims, n_rows: int, n_req: int, device):
+    With fuse_topk (the default where topk <= 16 and max_blocks <= 8704) scoring and
+    top-k run as msa_select_prefill and no scores are kept; otherwise msa_index_score
+    writes `scores` and msa_topk_blocks selects from them."""
+
+    def __init__(self, dims: Dims, n_rows: int, n_req: int, device, fuse_topk=None):
         self.dims, self.n_rows, self.n_req = dims, n_rows, n_req
         f = dict(device=device)
-        self.scores = torch.empty((n_rows, dims.G, dims.max_blocks), dtype=torch.float32, **f)
+        n_chunks = (dims.max_blocks + 127) // 128
+        if fuse_topk is None:
+            fuse_topk = dims.topk <= 16 and n_chunks * 15 <= 1024
+        self.fuse_topk = bool(fuse_topk)
+        if self.fuse_topk:
+            self.scores = None
+            self.sel_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_SELECT_PREFILL, n_rows, n_req, dims)),),
+                                      dtype=torch.uint8, **f)
+        else:
+            self.scores = torch.empty((n_rows, dims.G, dims.max_blocks), dtype=torch.float32, **f)
         self.sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, **f)
         n_keys = dims.G * n_req * dims.max_blocks
         self.blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, **f)
@@ -483,12 +529,17 @@ class PrefillStep:
         self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
         self.err = new_err_word(device)
-        self.kernel_launches = 10   # score, top-k, 4 inversion kernels (+ memset), plan, attention, merge
+        self.kernel_launches = 10   # score, top-k (or list merge), 4 inversion kernels (+ memset), plan,
+                                    # attention, merge
 
     def select(self, q_idx, kidx_cache, block_table, q_req, q_pos):
-        msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
-                        scores=self.scores, err_word=self.err)
-        msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
+        if self.fuse_topk:
+            msa_select_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, sel=self.sel,
+                               workspace=self.sel_ws, err_word=self.err)
+        else:
+            msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
+                            scores=self.scores, err_word=self.err)
+            msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
         msa_invert_selection(self.sel, q_req, self.n_req, self.dims, self.blk_off, self.blk_ent, self.ent_pos,
                              self.inv_ws, err_word=self.err)
 

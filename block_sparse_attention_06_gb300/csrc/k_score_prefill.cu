@@ -19,6 +19,11 @@
 //              written out by each warp for its own 32 rows as coalesced 128-byte
 //              row segments (no barrier across warps, so a timeout cannot leave a
 //              warp waiting for another).
+// With top-k fused in (section 未来工作 lists the small top-k kernel as a fusion
+// candidate) the epilogue writes no scores: each thread keeps its row's best
+// kListLen candidates of the chunk (top-k sort keys, blocks before the row's own
+// block) in registers and writes that list; a merge kernel then picks each
+// row's selection from the lists of all chunks.
 // All waits are bounded; a timeout raises MSA_FLAG_TIMEOUT and drains.
 #include "msa_device.cuh"
 #include "msa_internal.h"
@@ -29,6 +34,7 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kChunk = 128;            // blocks per CTA
 constexpr int kThreads = 192;
+constexpr int kListLen = kSelectListLen;   // candidates kept per (row, chunk) with top-k fused: topk <= 16
 
 template <int DI>
 struct ScoreSmem {
@@ -50,12 +56,12 @@ struct ScoreSmem {
 };
 
 
-template <int DI>
+template <int DI, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
     const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req,
     const int32_t *__restrict__ q_pos, int n_rows, int n_req, int n_pages, int G, int max_blocks,
-    int n_chunks, float *__restrict__ scores, int32_t *err) {
+    int n_chunks, float *__restrict__ scores, uint64_t *__restrict__ lists, int32_t *err) {
     using Smem = ScoreSmem<DI>;
     constexpr uint32_t kSw = DI == 64 ? 2u : 4u;           // descriptor swizzle: 128B / 64B
     constexpr uint32_t kSbo = 8u * DI * 2u;                // 8 rows of DI bf16
@@ -154,7 +160,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             for (int j = from + e; j < j_end_chunk; j += 128) o[j] = -INFINITY;
         }
     };
+    // fused top-k: this chunk's candidate list of row i, kListLen keys (0 = none)
+    auto list_of = [&](int i) { return lists + ((size_t(row0 + i) * G + g) * n_chunks + chunk) * kListLen; };
     if (total <= 0) {
+        if (FUSED) {
+            if (tid < 128 && row0 + tid < n_rows)
+                for (int i = 0; i < kListLen; ++i) list_of(tid)[i] = 0ull;
+            return;
+        }
         fill_neg_inf();
         return;
     }
@@ -247,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
         const uint32_t lane_addr = tmem + (uint32_t(quad * 32) << 16);
         bool ok = true;
         int it = 0;                                      // blocks over all passes
+        const int own = p >> 7;                          // the row's own block (forced, not ranked)
+        uint64_t lst[kListLen];                          // fused top-k: best keys first, 0 = none
+#pragma unroll
+        for (int i = 0; i < kListLen; ++i) lst[i] = 0ull;
         for (int pk = 0; ok && pk < n_pass; ++pk) {
         const int req = sm.pass_req[pk], nblk = pass_end(pk) - j0;
         for (int jj = 0; jj < nblk; ++jj, ++it) {
@@ -273,6 +290,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+            if (FUSED) {
+                const int jb = j0 + jj;
+                if (jb < own && (one_req || sm.row_req[row] == req)) {
+                    uint64_t key = topk_key(best, jb, err);
+                    if (key > lst[kListLen - 1]) {
+                        // sorted insertion: the key sinks to its place, the worst key drops out
+#pragma unroll
+                        for (int i = 0; i < kListLen; ++i) {
+                            const uint64_t cur = lst[i];
+                            const bool take = key > cur;
+                            lst[i] = take ? key : cur;
+                            key = take ? cur : key;
+                        }
+                    }
+                }
+                continue;
+            }
             sm.sc[row][jj & 31] = best;
             if ((jj & 31) == 31 || jj == nblk - 1) {
                 // the warp writes back its own 32 rows, one coalesced 128-byte segment per row
@@ -289,19 +323,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             }
         }
         }
+        if (FUSED && grow < n_rows) {
+            uint64_t *o = list_of(row);
+#pragma unroll
+            for (int i = 0; i < kListLen; ++i) o[i] = lst[i];
+        }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    fill_neg_inf();
+    if (!FUSED) fill_neg_inf();
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-template <int DI>
+template <int DI, bool FUSED>
 cudaError_t launch_di(const void *q_idx, const void *kidx, const int32_t *bt, const int32_t *q_req,
                       const int32_t *q_pos, int n_rows, int n_req, int n_pages, const Shape &s, float *scores,
-                      int32_t *err, cudaStream_t st) {
+                      uint64_t *lists, int32_t *err, cudaStream_t st) {
     alignas(64) CUtensorMap am, bm;
     const char *why = nullptr;
     {
@@ -319,13 +358,14 @@ cudaError_t launch_di(const void *q_idx, const void *kidx, const int32_t *bt, co
     const int n_tiles = (n_rows + 127) / 128;
     const int n_chunks = (s.max_blocks + kChunk - 1) / kChunk;
     const size_t smem = sizeof(ScoreSmem<DI>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_score_prefill<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e =
+        cudaFuncSetAttribute(k_score_prefill<DI, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     const long long gx = 1LL * n_tiles * n_chunks;
     if (gx > 0x7fffffffLL || s.G > 65535) return cudaErrorInvalidConfiguration;
     dim3 grid(unsigned(gx), unsigned(s.G));
-    k_score_prefill<DI><<<grid, kThreads, smem, st>>>(am, bm, bt, q_req, q_pos, n_rows, n_req, n_pages, s.G,
-                                                      s.max_blocks, n_chunks, scores, err);
+    k_score_prefill<DI, FUSED><<<grid, kThreads, smem, st>>>(am, bm, bt, q_req, q_pos, n_rows, n_req, n_pages,
+                                                             s.G, s.max_blocks, n_chunks, scores, lists, err);
     return cudaGetLastError();
 }
 
@@ -333,13 +373,20 @@ cudaError_t launch_di(const void *q_idx, const void *kidx, const int32_t *bt, co
 
 cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int32_t *block_table,
                                  const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
-                                 int n_pages, const Shape &s, float *scores, int32_t *err, cudaStream_t st) {
+                                 int n_pages, const Shape &s, float *scores, uint64_t *lists, int32_t *err,
+                                 cudaStream_t st) {
     if (n_rows <= 0) return cudaSuccess;
-    if (s.Di == 64)
-        return launch_di<64>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores, err, st);
-    if (s.Di == 32)
-        return launch_di<32>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores, err, st);
+#define MSA_SP_CASE(DD)                                                                                          \
+    if (s.Di == DD)                                                                                              \
+        return lists ? launch_di<DD, true>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s,    \
+                                           scores, lists, err, st)                                               \
+                     : launch_di<DD, false>(q_idx, kidx, block_table, q_req, q_pos, n_rows, n_req, n_pages, s,   \
+                                            scores, lists, err, st);
+    MSA_SP_CASE(64) MSA_SP_CASE(32)
+#undef MSA_SP_CASE
     return cudaErrorNotSupported;
 }
+
+int score_prefill_chunks(int max_blocks) { return (max_blocks + kChunk - 1) / kChunk; }
 
 }  // namespace msa

@@ -13,18 +13,6 @@ namespace {
 
 // ------------------------------------------------------------------ top-k
 
-// Sort key: higher score first, lower block id on ties; -0.0 == +0.0.  Every
-// candidate key is non-zero (the low word is ~j with j < 2^31), so 0 marks "none".
-__device__ __forceinline__ uint64_t block_key(float s, int j, int32_t *err) {
-    if (s != s) {
-        raise_flag(err, MSA_FLAG_NAN);
-        s = -INFINITY;
-    }
-    const uint32_t u = __float_as_uint(s == 0.0f ? 0.0f : s);
-    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    return (uint64_t(ord) << 32) | uint64_t(~uint32_t(j));
-}
-
 __device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
 // Largest of a lane's keys that is below `bound` (0 when none): four independent
@@ -119,7 +107,45 @@ __global__ void __launch_bounds__(256) k_topk_warp(const float *__restrict__ sco
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int j = lane + 32 * i;
-        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+        keys[i] = j < own ? topk_key(s[j], j, err) : 0ull;
+    }
+    const int mine = int(~uint32_t(warp_top_n<PER>(keys, k_eff - 1)));
+    const int rank = rank_ascending(mine, k_eff - 1);
+    if (lane < k_eff - 1) out[rank] = mine;
+    if (lane == 0) out[k_eff - 1] = own;
+    for (int i = k_eff + lane; i < topk; i += 32) out[i] = -1;
+}
+
+// Top-k fused into prefill scoring, second half: one warp per (row, group) merges the
+// candidate lists that the scoring CTAs kept for the row's block chunks (the best
+// kSelectListLen keys of each chunk, 0 = none) into the selection, with the same
+// rule and output as k_topk_warp.  The lists hold every candidate that can make
+// the row's top k - 1, so the selection is the one k_topk_warp makes from the
+// scores.
+template <int PER>
+__global__ void __launch_bounds__(256) k_topk_merge(const uint64_t *__restrict__ lists,
+                                                    const int32_t *__restrict__ q_pos, int n_rows, int G,
+                                                    int max_blocks, int n_cand, int topk,
+                                                    int32_t *__restrict__ sel, int32_t *err) {
+    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (item >= n_rows * G) return;
+    const int r = item / G;
+    int32_t *out = sel + size_t(item) * topk;
+    const int p = q_pos[r];
+    if (p < 0 || (p >> 7) >= max_blocks) {
+        for (int i = lane; i < topk; i += 32) out[i] = -1;
+        if (lane == 0) raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const uint64_t *l = lists + size_t(item) * n_cand;
+    uint64_t keys[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int c = lane + 32 * i;
+        keys[i] = c < n_cand ? l[c] : 0ull;
     }
     const int mine = int(~uint32_t(warp_top_n<PER>(keys, k_eff - 1)));
     const int rank = rank_ascending(mine, k_eff - 1);
@@ -153,7 +179,7 @@ __global__ void __launch_bounds__(NT) k_topk_cta(const float *__restrict__ score
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int j = tid + NT * i;
-        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+        keys[i] = j < own ? topk_key(s[j], j, err) : 0ull;
     }
     const uint64_t best = cta_top_n<NT, PER>(keys, k_eff - 1, stage);
     if (tid < 32) {
@@ -246,7 +272,7 @@ __global__ void __launch_bounds__(256) k_decode_select_warp(
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int j = lane + 32 * i;
-        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+        keys[i] = j < own ? topk_key(s[j], j, err) : 0ull;
     }
     const uint64_t best = warp_top_n<PER>(keys, k_eff - 1);
     emit_decode_row(best, item, b, L, own, k_eff, topk, max_blocks, n_pages, block_table, sel, pt, row_len, err);
@@ -286,7 +312,7 @@ __global__ void __launch_bounds__(NT) k_decode_select_cta(
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const int j = tid + NT * i;
-        keys[i] = j < own ? block_key(s[j], j, err) : 0ull;
+        keys[i] = j < own ? topk_key(s[j], j, err) : 0ull;
     }
     const uint64_t best = cta_top_n<NT, PER>(keys, k_eff - 1, stage);
     if (tid < 32)
@@ -456,6 +482,23 @@ __global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, size_t words, si
 }
 
 }  // namespace
+
+cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n_rows, const Shape &s,
+                              int n_chunks, int32_t *sel, int32_t *err, cudaStream_t st) {
+    if (n_rows <= 0) return cudaSuccess;
+    const int n_cand = n_chunks * kSelectListLen;
+    const long long warps = 1LL * n_rows * s.G;
+    const unsigned blocks = unsigned((warps + 7) / 8);
+#define MSA_TM_CASE(PP)                                                                                     \
+    if (n_cand <= 32 * PP) {                                                                                \
+        k_topk_merge<PP><<<blocks, 256, 0, st>>>(lists, q_pos, n_rows, s.G, s.max_blocks, n_cand, s.topk, sel, \
+                                                 err);                                                      \
+        return cudaGetLastError();                                                                          \
+    }
+    MSA_TM_CASE(1) MSA_TM_CASE(2) MSA_TM_CASE(3) MSA_TM_CASE(4) MSA_TM_CASE(8) MSA_TM_CASE(16) MSA_TM_CASE(32)
+#undef MSA_TM_CASE
+    return cudaErrorNotSupported;
+}
 
 cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, const Shape &s,
                         int32_t *sel, int32_t *err, cudaStream_t st) {

@@ -150,13 +150,43 @@ msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const in
                                 err_word, cs);
     else if (phase == MSA_PHASE_PREFILL)
         e = launch_score_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores,
-                                 err_word, cs);
+                                 nullptr, err_word, cs);
     else if (phase == MSA_PHASE_DECODE_MULTI)
         e = launch_score_decode_mt(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, scores,
                                    err_word, cs);
     else
         return fail(MSA_ERR_INVALID_ARG, "msa_index_score: unknown phase %d", phase);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_score");
+}
+
+msa_status_t msa_select_prefill(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
+                                const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
+                                int32_t n_pages, const msa_dims_t *dims, int32_t *sel, void *workspace,
+                                size_t workspace_bytes, int32_t *err_word, msa_stream_t stream) {
+    Shape s;
+    msa_status_t st = check_dims(dims, false, true, &s, "msa_select_prefill");
+    if (st != MSA_OK) return st;
+    MSA_REQUIRE(n_rows >= 0 && n_req > 0 && n_pages > 0, "msa_select_prefill: bad sizes");
+    if (n_rows == 0) return MSA_OK;
+    MSA_REQUIRE(q_idx && kidx_cache && block_table && q_req && q_pos && sel && workspace && err_word,
+                "msa_select_prefill: NULL pointer");
+    const int n_chunks = score_prefill_chunks(s.max_blocks);
+    if (s.topk > kSelectListLen + 1)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_select_prefill: topk > %d", kSelectListLen + 1);
+    if (n_chunks * kSelectListLen > 1024)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_select_prefill: max_blocks > %d", 1024 / kSelectListLen * 128);
+    const size_t need = size_t(n_rows) * s.G * n_chunks * kSelectListLen * sizeof(uint64_t);
+    if (workspace_bytes < need)
+        return fail(MSA_ERR_WORKSPACE, "msa_select_prefill: workspace of %zu bytes, %zu needed", workspace_bytes,
+                    need);
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+        return fail(MSA_ERR_INVALID_ARG, "msa_select_prefill: workspace must be 16-byte aligned");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    uint64_t *lists = static_cast<uint64_t *>(workspace);
+    cudaError_t e = launch_score_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s,
+                                         nullptr, lists, err_word, cs);
+    if (e == cudaSuccess) e = launch_topk_merge(lists, q_pos, n_rows, s, n_chunks, sel, err_word, cs);
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_select_prefill");
 }
 
 msa_status_t msa_topk_blocks(const float *scores, const int32_t *q_pos, int32_t n_rows, const msa_dims_t *dims,
@@ -348,6 +378,10 @@ size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_
     if (op == MSA_OP_PREFILL) {
         if (check_dims(dims, true, false, &s, "msa_workspace_bytes") != MSA_OK || n_req <= 0) return 0;
         return prefill_workspace_bytes(n_rows, n_req, s);
+    }
+    if (op == MSA_OP_SELECT_PREFILL) {
+        if (check_dims(dims, false, true, &s, "msa_workspace_bytes") != MSA_OK) return 0;
+        return size_t(n_rows) * s.G * score_prefill_chunks(s.max_blocks) * kSelectListLen * sizeof(uint64_t);
     }
     return 0;
 }

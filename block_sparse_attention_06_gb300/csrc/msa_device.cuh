@@ -44,6 +44,22 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     return v;
 }
 
+// ------------------------------------------------------------------ top-k keys
+
+// Sort key of candidate block j with score s for the top-k selection: higher score
+// first, lower block id on ties; -0.0 ranks equal to +0.0; a NaN raises MSA_FLAG_NAN
+// and ranks as -inf.  Every candidate key is non-zero (the low word is ~j with
+// j < 2^31), so 0 marks "no candidate".
+__device__ __forceinline__ uint64_t topk_key(float s, int j, int32_t *err) {
+    if (s != s) {
+        raise_flag(err, MSA_FLAG_NAN);
+        s = -INFINITY;
+    }
+    const uint32_t u = __float_as_uint(s == 0.0f ? 0.0f : s);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (uint64_t(ord) << 32) | uint64_t(~uint32_t(j));
+}
+
 // ------------------------------------------------------------------ shared memory / mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -50,8 +50,14 @@ cudaError_t launch_score_decode_mt(const void *q_idx, const void *kidx, const in
                                    const Shape &s, float *scores, int32_t *err, cudaStream_t st);
 cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int32_t *block_table,
                                  const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
-                                 int n_pages, const Shape &s, float *scores, int32_t *err,
+                                 int n_pages, const Shape &s, float *scores, uint64_t *lists, int32_t *err,
                                  cudaStream_t st);
+// Prefill scoring with top-k fused: block chunks per row (candidate lists per (row, group, chunk)),
+// candidates kept per list, and the merge of the lists into the selection.
+int score_prefill_chunks(int max_blocks);
+constexpr int kSelectListLen = 15;
+cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n_rows, const Shape &s,
+                              int n_chunks, int32_t *sel, int32_t *err, cudaStream_t st);
 
 cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, const Shape &s,
                         int32_t *sel, int32_t *err, cudaStream_t st);

@@ -88,6 +88,7 @@ typedef void *msa_stream_t;
 #define MSA_OP_INVERT  0
 #define MSA_OP_DECODE  1
 #define MSA_OP_PREFILL 2
+#define MSA_OP_SELECT_PREFILL 3
 
 /*
  * msa_index_score -- block scores for every (row, group, candidate block).
@@ -123,6 +124,27 @@ msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const in
                              const int32_t *q_req, const int32_t *q_pos, int32_t n_rows,
                              int32_t n_req, int32_t n_pages, const msa_dims_t *dims, int32_t phase,
                              float *scores, int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_select_prefill -- msa_index_score (MSA_PHASE_PREFILL) and msa_topk_blocks in
+ * one pass, writing the same selection and no scores.  [T-zh 未来工作]: the small
+ * top-k kernel is a fusion candidate.  Each scoring CTA keeps, per row, the best
+ * topk - 1 candidates of its chunk of 128 blocks (the sort keys of
+ * msa_topk_blocks, in registers); a merge kernel picks each row's selection from
+ * the lists of all its chunks.
+ *
+ *   q_idx ... dims   as msa_index_score
+ *   sel       int32 [n_rows][G][topk]  out, identical to msa_topk_blocks on the
+ *             scores of msa_index_score
+ *   workspace device scratch of msa_workspace_bytes(MSA_OP_SELECT_PREFILL, n_rows,
+ *             n_req, dims) bytes, 16-byte aligned (the candidate lists)
+ * Limits: topk <= 16 and max_blocks <= 8704 (MSA_ERR_UNSUPPORTED otherwise: use
+ * the two calls).
+ */
+msa_status_t msa_select_prefill(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
+                                const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
+                                int32_t n_pages, const msa_dims_t *dims, int32_t *sel, void *workspace,
+                                size_t workspace_bytes, int32_t *err_word, msa_stream_t stream);
 
 /*
  * msa_topk_blocks -- per (row, group): the own block q_pos/128 is always kept;

@@ -19,9 +19,9 @@ def msa():
     return m
 
 
-def _run(m, case):
+def _run(m, case, fuse_topk=False):
     dims = m.dims_of(case)
-    step = m.PrefillStep(dims, case.n_rows, case.n_req, DEV)
+    step = m.PrefillStep(dims, case.n_rows, case.n_req, DEV, fuse_topk=fuse_topk)
     step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.q_req, case.q_pos)
     m.msa_check(step.err)
     torch.cuda.synchronize()
@@ -100,6 +100,35 @@ def test_prefill68k_sampled(msa):
     case = mi.named_case("prefill68k", device=DEV)
     rows = [0, 1, 127, 128, 255, 256, 1000, 4095, 4096, 6000, 8190, 8191]
     _check_prefill(msa, case, rows, check_partials=True)
+
+
+def _fused_cases():
+    yield "tiny", lambda: mi.tiny_case(seed=1000, device=DEV)[0]
+    yield "ragged", lambda: mi.prefill_case(1000, 300, Hq=16, G=2, D=128, Di=64, topk=6, pool_pages=40, seed=12,
+                                            device=DEV)
+    yield "one_row", lambda: mi.prefill_case(127, 1, Hq=16, G=2, D=128, Di=64, topk=6, pool_pages=40, seed=12,
+                                             device=DEV)
+    yield "multi_request", lambda: mi.ragged_prefill_case([0, 5000, 64, 130], [1, 300, 63, 200], Hq=8, G=2, D=64,
+                                                          Di=32, topk=6, pool_pages=120, seed=21, device=DEV)
+    yield "g8_k16", lambda: mi.prefill_case(2100, 400, Hq=32, G=8, D=128, Di=64, topk=16, pool_pages=40, seed=13,
+                                            device=DEV)
+    yield "prefill68k", lambda: mi.named_case("prefill68k", device=DEV)
+
+
+@pytest.mark.parametrize("name,make", list(_fused_cases()), ids=[n for n, _ in _fused_cases()])
+def test_fused_select_equals_score_then_topk(msa, name, make):
+    """msa_select_prefill (top-k fused into scoring) selects exactly what msa_index_score +
+    msa_topk_blocks select, so the whole prefill step gives identical bits."""
+    case = make()
+    unfused = _run(msa, case, fuse_topk=False)
+    fused = _run(msa, case, fuse_topk=True)
+    assert fused.fuse_topk and fused.scores is None
+    assert torch.equal(fused.sel, unfused.sel)
+    n_ent = int(unfused.blk_off[-1])        # entries past the CSR's end are scratch
+    assert torch.equal(fused.blk_off, unfused.blk_off)
+    assert torch.equal(fused.blk_ent[:n_ent], unfused.blk_ent[:n_ent])
+    assert torch.equal(fused.out, unfused.out)
+    assert torch.equal(fused.lse, unfused.lse)
 
 
 def test_topk_bit_exact_on_oracle_scores(msa):
