@@ -109,13 +109,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// Three-input fp32 maximum (one instruction on sm_100-class SMs).
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 // Two fp32 lanes per instruction (the f32x2 datapath of sm_100-class SMs); b2 / c2 hold one value
 // in both halves.
 __device__ __forceinline__ uint64_t dup2(float x) {

@@ -272,21 +272,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             if (!ok) break;
             tc_fence_after();
             const int lim = p - (j0 + jj) * 128;     // columns c <= lim are visible
-            float best = -INFINITY;
+            // block max in four independent chains of 3-input maxima (one dependent chain would
+            // leave the epilogue waiting on instruction latency)
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(lane_addr + uint32_t(acc * 128 + c0), v);
                 tmem_ld_wait();
-                if (lim >= c0 + 31) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) best = fmaxf(best, __uint_as_float(v[i]));
-                } else {
+                if (lim < c0 + 31) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        best = fmaxf(best, (c0 + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                        if (c0 + i > lim) v[i] = __float_as_uint(-INFINITY);
                 }
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mx[k] = fmax3(mx[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 4 + k]));
             }
+            const float best = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);

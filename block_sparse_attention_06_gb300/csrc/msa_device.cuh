@@ -44,6 +44,13 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void *p) {
     return v;
 }
 
+// Three-input fp32 maximum (one instruction on sm_100-class SMs).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ------------------------------------------------------------------ top-k keys
 
 // Sort key of candidate block j with score s for the top-k selection: higher score
