@@ -359,16 +359,18 @@ __global__ void k_page_table(const int32_t *__restrict__ sel, const int32_t *__r
 // ascending order.  Deterministic for any schedule.
 
 struct InvLayout {
-    size_t n_keys, words, bitmap_off, cnt_off, bytes;
+    size_t n_keys, words, bitmap_off, prefix_off, cnt_off, bytes;
 };
 
+// Workspace: the per-key row bitmap, the per-key exclusive prefix count of its words, the per-key count.
 __host__ __device__ inline InvLayout inv_layout(int n_rows, int n_req, int G, int max_blocks) {
     InvLayout l;
     l.n_keys = size_t(G) * n_req * max_blocks;
     l.words = (size_t(n_rows) + 31) / 32;
     l.bitmap_off = 0;
-    size_t bm = l.n_keys * l.words * 4;
-    l.cnt_off = (bm + 255) & ~size_t(255);
+    const size_t bm = (l.n_keys * l.words * 4 + 255) & ~size_t(255);
+    l.prefix_off = bm;
+    l.cnt_off = l.prefix_off + bm;
     l.bytes = l.cnt_off + ((l.n_keys * 4 + 255) & ~size_t(255));
     return l;
 }
@@ -393,16 +395,28 @@ __global__ void k_inv_mark(const int32_t *__restrict__ sel, const int32_t *__res
     if (old & bit) raise_flag(err, MSA_FLAG_BOUNDS);   // a block listed twice for one (row, group)
 }
 
+// One warp per key: the rows that selected the key (set bits), counted per bitmap word into an
+// exclusive prefix over the key's words, and in total.
 __global__ void k_inv_count(const uint32_t *__restrict__ bitmap, size_t words, size_t n_keys,
-                            int32_t *__restrict__ cnt) {
+                            int32_t *__restrict__ prefix, int32_t *__restrict__ cnt) {
     const size_t key = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (key >= n_keys) return;
     const uint32_t *row = bitmap + key * words;
-    int c = 0;
-    for (size_t w = lane; w < words; w += 32) c += __popc(row[w]);
-    c = warp_sum_i(c);
-    if (lane == 0) cnt[key] = c;
+    int32_t *pre = prefix + key * words;
+    int base = 0;
+    for (size_t w0 = 0; w0 < words; w0 += 32) {
+        const int c = (w0 + lane < words) ? __popc(row[w0 + lane]) : 0;
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (w0 + lane < words) pre[w0 + lane] = base + x - c;
+        base += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) cnt[key] = base;
 }
 
 // Exclusive scan of n counts into off[0..n] with one CTA of 1024 threads.
@@ -444,41 +458,30 @@ __global__ void __launch_bounds__(1024) k_inv_scan(const int32_t *__restrict__ c
     if (tid == 0) off[n] = carry_s;
 }
 
-__global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, size_t words, size_t n_keys,
-                           const int32_t *__restrict__ off, const int32_t *__restrict__ sel, int n_req,
-                           int G, int topk, int max_blocks, int32_t *__restrict__ ent,
-                           int32_t *__restrict__ ent_pos) {
-    const size_t key = (size_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (key >= n_keys) return;
-    const int g = int(key / (size_t(n_req) * max_blocks));
-    const int j = int(key % size_t(max_blocks));
-    const uint32_t *row = bitmap + key * words;
-    int32_t base = off[key];
-    for (size_t w0 = 0; w0 < words; w0 += 32) {
-        const uint32_t word = (w0 + lane < words) ? row[w0 + lane] : 0u;
-        const int c = __popc(word);
-        int x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        int pos = base + x - c;
-        uint32_t bits = word;
-        while (bits) {
-            const int b = __ffs(bits) - 1;
-            bits &= bits - 1;
-            const int q = int((w0 + lane) * 32 + b);
-            const int32_t *sq = sel + (size_t(q) * G + g) * topk;
-            int slot = 0;
-            for (int s = 0; s < topk; ++s)
-                if (sq[s] == j) slot = s;
-            ent_pos[(size_t(q) * G + g) * topk + slot] = pos;
-            ent[pos++] = q * topk + slot;
-        }
-        base += __shfl_sync(0xffffffffu, x, 31);
+// One thread per (row q, group g, slot): its place among the rows that selected the same key is
+// the key's CSR offset, the set bits of the key's bitmap in the words before q's word, and those
+// of q's word below bit q (rows ascending: the order is stable in q and does not depend on the
+// schedule).  Empty or rejected slots get ent_pos -1.
+__global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, const int32_t *__restrict__ prefix, size_t words,
+                           const int32_t *__restrict__ off, const int32_t *__restrict__ sel,
+                           const int32_t *__restrict__ q_req, int n_rows, int n_req, int G, int topk,
+                           int max_blocks, int32_t *__restrict__ ent, int32_t *__restrict__ ent_pos) {
+    const size_t e = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= size_t(n_rows) * G * topk) return;
+    const int j = sel[e];
+    const int q = int(e / (size_t(G) * topk));
+    const int g = int((e / topk) % G);
+    const int slot = int(e % topk);
+    const int req = q_req[q];
+    if (j < 0 || j >= max_blocks || req < 0 || req >= n_req) {   // bounds were flagged by k_inv_mark
+        ent_pos[e] = -1;
+        return;
     }
+    const size_t key = (size_t(g) * n_req + req) * max_blocks + j;
+    const size_t w = key * words + (q >> 5);
+    const int pos = off[key] + prefix[w] + __popc(bitmap[w] & ((1u << (q & 31)) - 1u));
+    ent[pos] = q * topk + slot;
+    ent_pos[e] = pos;
 }
 
 }  // namespace
@@ -572,6 +575,7 @@ cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, 
     const InvLayout l = inv_layout(n_rows, n_req, s.G, s.max_blocks);
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(w + l.bitmap_off);
+    int32_t *prefix = reinterpret_cast<int32_t *>(w + l.prefix_off);
     int32_t *cnt = reinterpret_cast<int32_t *>(w + l.cnt_off);
     cudaError_t e = cudaMemsetAsync(bitmap, 0, l.n_keys * l.words * 4, st);
     if (e != cudaSuccess) return e;
@@ -581,10 +585,12 @@ cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, 
                                                                    s.max_blocks, bitmap, l.words, err);
     }
     const unsigned kgrid = unsigned((l.n_keys + 7) / 8);
-    k_inv_count<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, cnt);
+    k_inv_count<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, prefix, cnt);
     k_inv_scan<<<1, 1024, 0, st>>>(cnt, l.n_keys, blk_off);
-    k_inv_emit<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, blk_off, sel, n_req, s.G, s.topk,
-                                      s.max_blocks, blk_ent, ent_pos);
+    if (n_ent > 0)
+        k_inv_emit<<<unsigned((n_ent + 255) / 256), 256, 0, st>>>(bitmap, prefix, l.words, blk_off, sel, q_req,
+                                                                   n_rows, n_req, s.G, s.topk, s.max_blocks,
+                                                                   blk_ent, ent_pos);
     return cudaGetLastError();
 }
 

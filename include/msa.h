@@ -195,7 +195,7 @@ msa_status_t msa_build_page_table(const int32_t *sel, const int32_t *block_table
  *   blk_ent  int32 [n_rows * G * topk]           out (first blk_off[last] used)
  *   ent_pos  int32 [n_rows][G][topk]             out; blk_ent[ent_pos[q][g][s]] ==
  *                                                q * topk + s where sel[q][g][s] >= 0,
- *                                                unwritten where sel < 0
+ *                                                -1 where sel < 0
  *   workspace device scratch of msa_workspace_bytes(MSA_OP_INVERT, ...) bytes
  */
 msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int32_t n_rows,

@@ -100,7 +100,8 @@ def test_workspace_sizes_and_errors(lib):
     d = good_dims(max_blocks=533)
     inv = lib.msa_workspace_bytes(0, 8192, 1, ctypes.byref(d))
     # bitmap over (group, block) keys x ceil(rows/32) words + per-key counts, 256-byte aligned
-    assert inv == ((8 * 533 * 256 * 4 + 255) // 256) * 256 + ((8 * 533 * 4 + 255) // 256) * 256
+    # bitmap and per-word prefix counts (one int32 per key and 32 rows each), then one count per key
+    assert inv == 2 * (((8 * 533 * 256 * 4 + 255) // 256) * 256) + ((8 * 533 * 4 + 255) // 256) * 256
     dec = lib.msa_workspace_bytes(1, 8, 0, ctypes.byref(good_dims()))
     # fp32 partials + their lse + one merge counter per (request, group) row, 256-byte aligned
     assert dec == (((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
