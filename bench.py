@@ -31,10 +31,10 @@ if ROOT not in sys.path:
 
 METRIC = "MSA decode tok/s & prefill q-tok/s at 60k ctx; % of HBM / tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per launch from the committed ncu summaries
-# (profiles/k_score_decode__decode60k.md); None when no capture of the current
-# kernel on the bench workload exists.
-NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": None}
+# DRAM bytes (read + write) per launch, from one-pass ncu captures
+# (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels on the
+# bench workloads; None when no capture of the current kernel exists.
+NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2976990000}
 
 
 def parse_args():

@@ -11,10 +11,11 @@
 //     m16n8k16 bf16 MMA (tokens = M), the way the page's own index-scoring kernel
 //     uses 128-token tiles as M; decode attention moves ~8 flop per byte, so
 //     these small legacy tiles keep it HBM-bound;
-//   - each work item writes a normalised partial (O, lse) to the workspace and
-//     counts itself done on the row's counter; the work item that finishes a row
-//     last merges the row's partials by Log-Sum-Exp (the reduction of section
-//     KV 块主序稀疏注意力) and writes the output, so no second kernel runs.
+//   - each row segment (the row's pages inside one CTA's range) writes one
+//     normalised partial (O, lse) to the workspace and counts its pages done on
+//     the row's counter; the segment that completes a row merges the row's
+//     partials by Log-Sum-Exp (the reduction of section KV 块主序稀疏注意力) and
+//     writes the output, so no second kernel runs.
 #include "msa_device.cuh"
 #include "msa_internal.h"
 

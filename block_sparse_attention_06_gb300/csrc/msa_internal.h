@@ -85,7 +85,8 @@ cudaError_t launch_lse_merge(const void *o_part, const float *lse_part, const in
                              const int32_t *ent_pos, int n_rows, const Shape &s, void *out, float *lse,
                              int32_t *err, cudaStream_t st);
 
-// Decode workspace: split-by-page partials, their lse, and one merge counter per
+// Decode workspace: segment partials (one per run of a row's pages inside one
+// CTA's range, at the run's first slot), their lse, and one merge counter per
 // (request, group) row.  The counters must be zero when the attention kernel
 // starts; launch_attn_decode clears them itself unless counters_zeroed is set
 // (the fused decode step clears them in its select kernel).

@@ -6,7 +6,7 @@
 // later allocation through its own allocator.  Another is a plugin host that
 // forbids libraries from calling the CUDA allocator: cudaMalloc can synchronise
 // the device and fails once the pool is reserved.  Such callers also cannot hand
-// us a workspace.  This variant therefore keeps the split-by-page partials in a
+// us a workspace.  This variant therefore keeps the segment partials in a
 // file-scope device array of fixed size instead of a caller-provided workspace.
 //
 // The array exists once per GPU that loads the library and stays allocated until

@@ -257,10 +257,12 @@ msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int3
  * tables ([T-zh 将 MSA 与分页注意力集成]): row r = b * G + g reads its row_len[r]
  * tokens from pages page_table[r][0], [1], ... in order (slot s holds tokens
  * s*128 .. s*128+127 of the row); the Hq/G heads of group g attend them.
- * Split by page: one partial per (row, slot) in the workspace; the work item
- * that finishes a row last merges the row's partials (the same reduction as
- * msa_lse_merge), counted on a per-row counter in the workspace that this call
- * clears before its kernel runs.
+ * The (row, slot) items are cut into one contiguous range per SM; the slots of a
+ * row inside one range (a segment) share one online softmax and write one partial
+ * to the workspace, at the segment's first slot.  The segment that completes a
+ * row merges the row's partials (the same reduction as msa_lse_merge), counted
+ * in pages on a per-row counter in the workspace that this call clears before
+ * its kernel runs.
  *
  *   q          bf16 [B][Hq][D]
  *   page_table int32 [B*G][topk];  row_len int32 [B*G]
@@ -330,7 +332,7 @@ msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cac
  * to it; it exists for callers like a serving engine that has reserved almost all
  * HBM for its paged KV pool and routes every allocation through its own
  * allocator, or a plugin host that forbids libraries from calling cudaMalloc.
- * Such a caller cannot provide a workspace either, so the split-by-page partials
+ * Such a caller cannot provide a workspace either, so the segment partials
  * go to a fixed 16 MiB device array inside the library instead.
  *
  *   Arguments, layouts and outputs: as msa_sparse_attn_decode, minus the workspace.
