@@ -249,21 +249,21 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
     s1_bytes = decode_bytes(case)
     s1_gbs = s1_bytes / (s1_ms / 1e3) / 1e9
 
-    # ---------------- e2e through the public API: pinned host inputs in, result out
-    host_in = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table")}
-    dev_in = {n: torch.empty_like(getattr(case, n)) for n in host_in}
-    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    host_lse = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    # ---------------- e2e through the public API: pinned host inputs in, result out.
+    # The step's inputs sit packed in one page-locked buffer (msa.DecodeInputs) and go
+    # up in one copy; out and lse come back in one copy.
+    inputs = msa.DecodeInputs(dims, B, dev)
+    for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table"):
+        getattr(inputs, "h_" + n).copy_(getattr(case, n).cpu())
+    host_res, _ = step.host_results()
+    h2d = inputs.nbytes
+    d2h = host_res.numel()
 
     def e2e_step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        out, lse = step(dev_in["q"], dev_in["q_idx"], case.k_cache, case.v_cache, case.kidx_cache,
-                        dev_in["block_table"], dev_in["seq_lens"], dev_in["q_pos"])
-        host_out.copy_(out, non_blocking=True)
-        host_lse.copy_(lse, non_blocking=True)
+        inputs.upload()
+        step(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table,
+             inputs.seq_lens, inputs.q_pos)
+        step.download(host_res)
 
     for _ in range(W):
         e2e_step()

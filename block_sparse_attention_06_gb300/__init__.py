@@ -448,8 +448,9 @@ class DecodeStep:
         self.sel = torch.empty((B, dims.G, dims.topk), dtype=torch.int32, **f)
         self.page_table = torch.empty((B * dims.G, dims.topk), dtype=torch.int32, **f)
         self.row_len = torch.empty((B * dims.G,), dtype=torch.int32, **f)
-        self.out = torch.empty((B, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
-        self.lse = torch.empty((B, dims.Hq), dtype=torch.float32, **f)
+        # out and lse share one device buffer, so a step's results come back in one copy
+        self._out_buf, (self.out, self.lse) = _packed(
+            [((B, dims.Hq, dims.D), torch.bfloat16), ((B, dims.Hq), torch.float32)], device)
         self.workspace = torch.empty((max(1, msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)),),
                                      dtype=torch.uint8, **f)
         self.err = new_err_word(device)
@@ -491,6 +492,65 @@ class DecodeStep:
         msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, self.dims, self.scores,
                         self.sel, self.page_table, self.row_len, self.out, self.lse, self.workspace, self.err)
         return self.out, self.lse
+
+    def host_results(self):
+        """Page-locked host buffer laid out like the device (out, lse) buffer, with
+        its (out, lse) views; download() fills it."""
+        buf = torch.empty(self._out_buf.shape, dtype=torch.uint8).pin_memory()
+        return buf, _views(buf, [(tuple(self.out.shape), self.out.dtype), (tuple(self.lse.shape), self.lse.dtype)])
+
+    def download(self, host_buf):
+        """Queue one device-to-host copy of out and lse into host_buf (from host_results)."""
+        host_buf.copy_(self._out_buf, non_blocking=True)
+
+
+def _layout(specs):
+    """Byte offsets of tensors packed back to back, each on a 256-byte boundary."""
+    offs, n = [], 0
+    for shape, dtype in specs:
+        offs.append(n)
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        n += (nbytes + 255) // 256 * 256
+    return offs, max(n, 1)
+
+
+def _views(buf, specs):
+    offs, _ = _layout(specs)
+    out = []
+    for (shape, dtype), o in zip(specs, offs):
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        out.append(buf[o:o + nbytes].view(dtype).view(shape))
+    return out
+
+
+def _packed(specs, device):
+    _, n = _layout(specs)
+    buf = torch.empty((n,), dtype=torch.uint8, device=device)
+    return buf, _views(buf, specs)
+
+
+class DecodeInputs:
+    """The per-step inputs of a decode step for B requests -- q, q_idx, seq_lens,
+    q_pos and block_table -- packed in one page-locked host buffer and one device
+    buffer of the same layout, so a step's host-to-device traffic is a single copy
+    (upload) instead of one copy per tensor.  Fill the host views (h_q, ...), call
+    upload(), then pass the device views (q, ...) to DecodeStep."""
+
+    def __init__(self, dims: Dims, B: int, device):
+        specs = [((B, dims.Hq, dims.D), torch.bfloat16), ((B, dims.G, dims.Di), torch.bfloat16),
+                 ((B,), torch.int32), ((B,), torch.int32), ((B, dims.max_blocks), torch.int32)]
+        _, n = _layout(specs)
+        self.host = torch.empty((n,), dtype=torch.uint8).pin_memory()
+        self.h_q, self.h_q_idx, self.h_seq_lens, self.h_q_pos, self.h_block_table = _views(self.host, specs)
+        self.dev, (self.q, self.q_idx, self.seq_lens, self.q_pos, self.block_table) = _packed(specs, device)
+
+    @property
+    def nbytes(self) -> int:
+        return self.host.numel()
+
+    def upload(self):
+        """Queue one host-to-device copy of all inputs on the current stream."""
+        self.dev.copy_(self.host, non_blocking=True)
 
 
 class PrefillStep:

@@ -141,3 +141,23 @@ def test_package_import_fails_loudly_without_library(tmp_path):
     code = "import block_sparse_attention_06_gb300"
     res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
     assert res.returncode != 0 and "libmsa.so is not built" in res.stderr
+
+
+def test_packed_buffer_layout():
+    """The packed staging buffers of DecodeInputs and DecodeStep: each view starts on
+    a 256-byte boundary, views do not overlap, and each has its dtype and shape."""
+    import torch
+    import block_sparse_attention_06_gb300 as m
+    specs = [((8, 64, 128), torch.bfloat16), ((8, 8, 64), torch.bfloat16), ((8,), torch.int32), ((3,), torch.int32),
+             ((8, 469), torch.int32)]
+    offs, n = m._layout(specs)
+    assert offs == [0, 131072, 139264, 139520, 139776] and n == 139776 + 15104
+    buf = torch.zeros(n, dtype=torch.uint8)
+    views = m._views(buf, specs)
+    for (shape, dtype), v, o in zip(specs, views, offs):
+        assert v.shape == shape and v.dtype == dtype and v.is_contiguous()
+        assert v.data_ptr() - buf.data_ptr() == o and o % 256 == 0
+    for i, v in enumerate(views):   # writing one view leaves the others untouched
+        v.fill_(i + 1)
+    for i, v in enumerate(views):
+        assert bool((v == i + 1).all())

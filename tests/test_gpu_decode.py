@@ -124,3 +124,28 @@ def test_out_of_range_page_is_flagged(msa):
     step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table, case.seq_lens,
          case.q_pos)
     msa.msa_check(step.err)
+
+
+def test_packed_inputs_and_results(msa):
+    """DecodeInputs (one host-to-device copy of all step inputs) and DecodeStep.download
+    (one copy of out and lse) give the same bits as the step on separate tensors."""
+    case = mi.decode_case([700, 3000, 129], Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=80, needles_per_group=2,
+                          seed=11, device=DEV)
+    dims = msa.dims_of(case)
+    step = msa.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    out, lse = step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table,
+                    case.seq_lens, case.q_pos)
+    msa.msa_check(step.err)
+    ref_out, ref_lse = out.cpu(), lse.cpu()
+    inputs = msa.DecodeInputs(dims, case.n_rows, DEV)
+    for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table"):
+        getattr(inputs, "h_" + n).copy_(getattr(case, n).cpu())
+    host_res, (h_out, h_lse) = step.host_results()
+    step.out.zero_()
+    inputs.upload()
+    step(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table, inputs.seq_lens,
+         inputs.q_pos)
+    step.download(host_res)
+    torch.cuda.synchronize()
+    msa.msa_check(step.err)
+    assert torch.equal(h_out, ref_out) and torch.equal(h_lse, ref_lse)
