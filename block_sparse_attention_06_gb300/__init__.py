@@ -27,6 +27,7 @@ MSA_OP_INVERT = 0
 MSA_OP_DECODE = 1
 MSA_OP_PREFILL = 2
 MSA_OP_SELECT_PREFILL = 3
+MSA_OP_SELECT_INVERT_PREFILL = 4
 
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
           4: "MSA_ERR_DEVICE_BOUNDS", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_WORKSPACE",
@@ -233,6 +234,50 @@ def msa_build_page_table(sel, block_table, seq_lens, n_pages: int, dims: Dims, p
     _call("msa_build_page_table", _ptr(sel), _ptr(block_table), _ptr(seq_lens), B, n_pages, ctypes.byref(d),
           _ptr(page_table), _ptr(row_len), _ptr(err_word), _stream(dev))
     return page_table, row_len
+
+
+def msa_select_invert_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, dims: Dims, sel=None, blk_off=None,
+                              blk_ent=None, ent_pos=None, workspace=None, err_word=None):
+    """msa_select_prefill then msa_invert_selection in one call, the inversion's
+    marking pass done by the list merge -> (sel, blk_off, blk_ent, ent_pos); the
+    requests are the rows of block_table; topk <= 16."""
+    n_rows = q_idx.shape[0]
+    _req(q_idx, torch.bfloat16, "q_idx", (n_rows, dims.G, dims.Di))
+    _req(kidx_cache, torch.bfloat16, "kidx_cache")
+    if kidx_cache.dim() != 4 or tuple(kidx_cache.shape[1:]) != (dims.page_size, dims.G, dims.Di):
+        raise ValueError("kidx_cache must be [n_pages][128][G][Di]")
+    _req(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or block_table.shape[1] != dims.max_blocks:
+        raise ValueError("block_table must be [n_req][max_blocks]")
+    _req(q_req, torch.int32, "q_req", (n_rows,))
+    _req(q_pos, torch.int32, "q_pos", (n_rows,))
+    dev = q_idx.device
+    n_req = block_table.shape[0]
+    n_keys = dims.G * n_req * dims.max_blocks
+    if sel is None:
+        sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, device=dev)
+    if blk_off is None:
+        blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, device=dev)
+    if blk_ent is None:
+        blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, device=dev)
+    if ent_pos is None:
+        ent_pos = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, device=dev)
+    _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
+    _req(blk_off, torch.int32, "blk_off", (n_keys + 1,))
+    _req(blk_ent, torch.int32, "blk_ent")
+    if blk_ent.numel() < n_rows * dims.G * dims.topk:
+        raise ValueError("blk_ent too small")
+    _req(ent_pos, torch.int32, "ent_pos", (n_rows, dims.G, dims.topk))
+    need = msa_workspace_bytes(MSA_OP_SELECT_INVERT_PREFILL, n_rows, n_req, dims)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    _req(workspace, torch.uint8, "workspace")
+    err_word = new_err_word(dev) if err_word is None else err_word
+    d = dims.c()
+    _call("msa_select_invert_prefill", _ptr(q_idx), _ptr(kidx_cache), _ptr(block_table), _ptr(q_req), _ptr(q_pos),
+          n_rows, n_req, kidx_cache.shape[0], ctypes.byref(d), _ptr(sel), _ptr(blk_off), _ptr(blk_ent),
+          _ptr(ent_pos), _ptr(workspace), workspace.numel(), _ptr(err_word), _stream(dev))
+    return sel, blk_off, blk_ent, ent_pos
 
 
 def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_ent=None, ent_pos=None,
@@ -557,9 +602,10 @@ class PrefillStep:
     """One MSA prefill chunk: tensor-core index scoring -> top-k -> {q,blk}->{blk,q}
     inversion -> KV-block-major sparse attention -> LSE merge.
 
-    With fuse_topk (the default where topk <= 16 and max_blocks <= 8704) scoring and
-    top-k run as msa_select_prefill and no scores are kept; otherwise msa_index_score
-    writes `scores` and msa_topk_blocks selects from them."""
+    With fuse_topk (the default where topk <= 16 and max_blocks <= 8704) scoring,
+    top-k and the inversion run as msa_select_invert_prefill and no scores are kept;
+    otherwise msa_index_score writes `scores`, msa_topk_blocks selects from them and
+    msa_invert_selection inverts."""
 
     def __init__(self, dims: Dims, n_rows: int, n_req: int, device, fuse_topk=None):
         self.dims, self.n_rows, self.n_req = dims, n_rows, n_req
@@ -570,8 +616,9 @@ class PrefillStep:
         self.fuse_topk = bool(fuse_topk)
         if self.fuse_topk:
             self.scores = None
-            self.sel_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_SELECT_PREFILL, n_rows, n_req, dims)),),
-                                      dtype=torch.uint8, **f)
+            self.sel_ws = torch.empty(
+                (max(1, msa_workspace_bytes(MSA_OP_SELECT_INVERT_PREFILL, n_rows, n_req, dims)),),
+                dtype=torch.uint8, **f)
         else:
             self.scores = torch.empty((n_rows, dims.G, dims.max_blocks), dtype=torch.float32, **f)
         self.sel = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, **f)
@@ -579,8 +626,8 @@ class PrefillStep:
         self.blk_off = torch.empty((n_keys + 1,), dtype=torch.int32, **f)
         self.blk_ent = torch.empty((max(1, n_rows * dims.G * dims.topk),), dtype=torch.int32, **f)
         self.ent_pos = torch.empty((n_rows, dims.G, dims.topk), dtype=torch.int32, **f)
-        self.inv_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)),),
-                                  dtype=torch.uint8, **f)
+        self.inv_ws = None if self.fuse_topk else torch.empty(
+            (max(1, msa_workspace_bytes(MSA_OP_INVERT, n_rows, n_req, dims)),), dtype=torch.uint8, **f)
         self.attn_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)),),
                                    dtype=torch.uint8, **f)
         n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
@@ -589,17 +636,18 @@ class PrefillStep:
         self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
         self.err = new_err_word(device)
-        self.kernel_launches = 10   # score, top-k (or list merge), 4 inversion kernels (+ memset), plan,
-                                    # attention, merge
+        # fused: scoring, list merge (+ the inversion's marks), 3 inversion kernels, plan, attention, merge;
+        # otherwise scoring, top-k and 4 inversion kernels
+        self.kernel_launches = 8 if self.fuse_topk else 9
 
     def select(self, q_idx, kidx_cache, block_table, q_req, q_pos):
         if self.fuse_topk:
-            msa_select_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, sel=self.sel,
-                               workspace=self.sel_ws, err_word=self.err)
-        else:
-            msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
-                            scores=self.scores, err_word=self.err)
-            msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
+            msa_select_invert_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, self.sel,
+                                      self.blk_off, self.blk_ent, self.ent_pos, self.sel_ws, err_word=self.err)
+            return
+        msa_index_score(q_idx, kidx_cache, block_table, q_req, q_pos, self.dims, MSA_PHASE_PREFILL,
+                        scores=self.scores, err_word=self.err)
+        msa_topk_blocks(self.scores, q_pos, self.dims, sel=self.sel, err_word=self.err)
         msa_invert_selection(self.sel, q_req, self.n_req, self.dims, self.blk_off, self.blk_ent, self.ent_pos,
                              self.inv_ws, err_word=self.err)
 

@@ -696,6 +696,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         const int quad = warp & 3;                 // TMEM lanes this warp may access
         const int row = quad * 32 + lane;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        // the partials are read back only by the merge kernel: evict them from L2 before Q, K and V
+        const uint64_t store_policy = l2_policy_evict_first();
         for (int u = 0;; ++u) {
             const int slot = u % kRing;
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort))) break;
@@ -755,7 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     if (rows > 0 && (rows & R)) {
 #pragma unroll
                         for (int i = 0; i < NSUB; ++i)
-                            tma_store_2d(&omaps.box[bx], sm.stg + i * 16384 + r0 * 128, i * 64, ent0 * HPG + r0);
+                            tma_store_2d_hint(&omaps.box[bx], sm.stg + i * 16384 + r0 * 128, i * 64,
+                                              ent0 * HPG + r0, store_policy);
                         r0 += R;
                     }
                 }

@@ -122,11 +122,32 @@ __global__ void __launch_bounds__(256) k_topk_warp(const float *__restrict__ sco
 // rule and output as k_topk_warp.  The lists hold every candidate that can make
 // the row's top k - 1, so the selection is the one k_topk_warp makes from the
 // scores.
+// The inversion's first pass for one selected block j of (row q, group g): set bit q
+// of key (g * n_req + q_req[q]) * max_blocks + j in the per-key row bitmap.  A block
+// listed twice for one (row, group), or a request id out of range, raises
+// MSA_FLAG_BOUNDS.
+__device__ __forceinline__ void inv_mark_one(uint32_t *__restrict__ bitmap, size_t words,
+                                             const int32_t *__restrict__ q_req, int n_req, int max_blocks, int q,
+                                             int g, int j, int32_t *err) {
+    const int req = q_req[q];
+    if (j < 0 || j >= max_blocks || req < 0 || req >= n_req) {
+        raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const size_t key = (size_t(g) * n_req + req) * max_blocks + j;
+    const uint32_t bit = 1u << (q & 31);
+    const uint32_t old = atomicOr(bitmap + key * words + (q >> 5), bit);
+    if (old & bit) raise_flag(err, MSA_FLAG_BOUNDS);
+}
+
+// Merge of the chunks' candidate lists into the selection, one warp per (row,
+// group).  With mark.bitmap set it also marks the inversion bitmap for every
+// selected block (the inversion's first pass, fused here).
 template <int PER>
 __global__ void __launch_bounds__(256) k_topk_merge(const uint64_t *__restrict__ lists,
                                                     const int32_t *__restrict__ q_pos, int n_rows, int G,
                                                     int max_blocks, int n_cand, int topk,
-                                                    int32_t *__restrict__ sel, int32_t *err) {
+                                                    int32_t *__restrict__ sel, InvMark mark, int32_t *err) {
     const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (item >= n_rows * G) return;
@@ -152,6 +173,12 @@ __global__ void __launch_bounds__(256) k_topk_merge(const uint64_t *__restrict__
     if (lane < k_eff - 1) out[rank] = mine;
     if (lane == 0) out[k_eff - 1] = own;
     for (int i = k_eff + lane; i < topk; i += 32) out[i] = -1;
+    if (mark.bitmap) {
+        const int g = item - r * G;
+        if (lane < k_eff - 1)
+            inv_mark_one(mark.bitmap, mark.words, mark.q_req, mark.n_req, max_blocks, r, g, mine, err);
+        if (lane == 0) inv_mark_one(mark.bitmap, mark.words, mark.q_req, mark.n_req, max_blocks, r, g, own, err);
+    }
 }
 
 // One CTA of NT threads per (row, group) for long contexts: each warp keeps its
@@ -384,15 +411,7 @@ __global__ void k_inv_mark(const int32_t *__restrict__ sel, const int32_t *__res
     if (j < 0) return;
     const int q = int(e / (size_t(G) * topk));
     const int g = int((e / topk) % G);
-    const int req = q_req[q];
-    if (j >= max_blocks || req < 0 || req >= n_req) {
-        raise_flag(err, MSA_FLAG_BOUNDS);
-        return;
-    }
-    const size_t key = (size_t(g) * n_req + req) * max_blocks + j;
-    const uint32_t bit = 1u << (q & 31);
-    const uint32_t old = atomicOr(bitmap + key * words + (q >> 5), bit);
-    if (old & bit) raise_flag(err, MSA_FLAG_BOUNDS);   // a block listed twice for one (row, group)
+    inv_mark_one(bitmap, words, q_req, n_req, max_blocks, q, g, j, err);
 }
 
 // One warp per key: the rows that selected the key (set bits), counted per bitmap word into an
@@ -487,7 +506,7 @@ __global__ void k_inv_emit(const uint32_t *__restrict__ bitmap, const int32_t *_
 }  // namespace
 
 cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n_rows, const Shape &s,
-                              int n_chunks, int32_t *sel, int32_t *err, cudaStream_t st) {
+                              int n_chunks, int32_t *sel, const InvMark &mark, int32_t *err, cudaStream_t st) {
     if (n_rows <= 0) return cudaSuccess;
     const int n_cand = n_chunks * kSelectListLen;
     const long long warps = 1LL * n_rows * s.G;
@@ -495,7 +514,7 @@ cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n
 #define MSA_TM_CASE(PP)                                                                                     \
     if (n_cand <= 32 * PP) {                                                                                \
         k_topk_merge<PP><<<blocks, 256, 0, st>>>(lists, q_pos, n_rows, s.G, s.max_blocks, n_cand, s.topk, sel, \
-                                                 err);                                                      \
+                                                 mark, err);                                                \
         return cudaGetLastError();                                                                          \
     }
     MSA_TM_CASE(1) MSA_TM_CASE(2) MSA_TM_CASE(3) MSA_TM_CASE(4) MSA_TM_CASE(8) MSA_TM_CASE(16) MSA_TM_CASE(32)
@@ -569,21 +588,37 @@ size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s) {
     return inv_layout(n_rows, n_req, s.G, s.max_blocks).bytes;
 }
 
+InvMark invert_clear(const int32_t *q_req, int n_rows, int n_req, const Shape &s, void *ws, cudaStream_t st,
+                     cudaError_t *e) {
+    const InvLayout l = inv_layout(n_rows, n_req, s.G, s.max_blocks);
+    InvMark m{reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + l.bitmap_off), l.words, q_req, n_req};
+    *e = cudaMemsetAsync(m.bitmap, 0, l.n_keys * l.words * 4, st);
+    return m;
+}
+
 cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
                           const Shape &s, int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws,
                           int32_t *err, cudaStream_t st) {
+    cudaError_t e;
+    const InvMark m = invert_clear(q_req, n_rows, n_req, s, ws, st, &e);
+    if (e != cudaSuccess) return e;
+    const size_t n_ent = size_t(n_rows) * s.G * s.topk;
+    if (n_ent > 0) {
+        k_inv_mark<<<unsigned((n_ent + 255) / 256), 256, 0, st>>>(sel, q_req, n_rows, n_req, s.G, s.topk,
+                                                                   s.max_blocks, m.bitmap, m.words, err);
+    }
+    return launch_invert_finish(sel, q_req, n_rows, n_req, s, blk_off, blk_ent, ent_pos, ws, err, st);
+}
+
+cudaError_t launch_invert_finish(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req, const Shape &s,
+                                 int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws, int32_t *err,
+                                 cudaStream_t st) {
     const InvLayout l = inv_layout(n_rows, n_req, s.G, s.max_blocks);
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(w + l.bitmap_off);
     int32_t *prefix = reinterpret_cast<int32_t *>(w + l.prefix_off);
     int32_t *cnt = reinterpret_cast<int32_t *>(w + l.cnt_off);
-    cudaError_t e = cudaMemsetAsync(bitmap, 0, l.n_keys * l.words * 4, st);
-    if (e != cudaSuccess) return e;
     const size_t n_ent = size_t(n_rows) * s.G * s.topk;
-    if (n_ent > 0) {
-        k_inv_mark<<<unsigned((n_ent + 255) / 256), 256, 0, st>>>(sel, q_req, n_rows, n_req, s.G, s.topk,
-                                                                   s.max_blocks, bitmap, l.words, err);
-    }
     const unsigned kgrid = unsigned((l.n_keys + 7) / 8);
     k_inv_count<<<kgrid, 256, 0, st>>>(bitmap, l.words, l.n_keys, prefix, cnt);
     k_inv_scan<<<1, 1024, 0, st>>>(cnt, l.n_keys, blk_off);

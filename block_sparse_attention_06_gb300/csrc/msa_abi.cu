@@ -159,22 +159,34 @@ msa_status_t msa_index_score(const void *q_idx, const void *kidx_cache, const in
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_score");
 }
 
+// Candidate lists of the fused prefill selection, 256-byte rounded.
+static size_t select_lists_bytes(int n_rows, const Shape &s) {
+    const size_t b = size_t(n_rows) * s.G * score_prefill_chunks(s.max_blocks) * kSelectListLen * sizeof(uint64_t);
+    return (b + 255) & ~size_t(255);
+}
+
+// Checks shared by msa_select_prefill and msa_select_invert_prefill.
+static msa_status_t check_select_prefill(const msa_dims_t *dims, Shape *s, const char *who) {
+    msa_status_t st = check_dims(dims, false, true, s, who);
+    if (st != MSA_OK) return st;
+    if (s->topk > kSelectListLen + 1) return fail(MSA_ERR_UNSUPPORTED, "%s: topk > %d", who, kSelectListLen + 1);
+    if (score_prefill_chunks(s->max_blocks) * kSelectListLen > 1024)
+        return fail(MSA_ERR_UNSUPPORTED, "%s: max_blocks > %d", who, 1024 / kSelectListLen * 128);
+    return MSA_OK;
+}
+
 msa_status_t msa_select_prefill(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
                                 const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
                                 int32_t n_pages, const msa_dims_t *dims, int32_t *sel, void *workspace,
                                 size_t workspace_bytes, int32_t *err_word, msa_stream_t stream) {
     Shape s;
-    msa_status_t st = check_dims(dims, false, true, &s, "msa_select_prefill");
+    msa_status_t st = check_select_prefill(dims, &s, "msa_select_prefill");
     if (st != MSA_OK) return st;
     MSA_REQUIRE(n_rows >= 0 && n_req > 0 && n_pages > 0, "msa_select_prefill: bad sizes");
     if (n_rows == 0) return MSA_OK;
     MSA_REQUIRE(q_idx && kidx_cache && block_table && q_req && q_pos && sel && workspace && err_word,
                 "msa_select_prefill: NULL pointer");
     const int n_chunks = score_prefill_chunks(s.max_blocks);
-    if (s.topk > kSelectListLen + 1)
-        return fail(MSA_ERR_UNSUPPORTED, "msa_select_prefill: topk > %d", kSelectListLen + 1);
-    if (n_chunks * kSelectListLen > 1024)
-        return fail(MSA_ERR_UNSUPPORTED, "msa_select_prefill: max_blocks > %d", 1024 / kSelectListLen * 128);
     const size_t need = size_t(n_rows) * s.G * n_chunks * kSelectListLen * sizeof(uint64_t);
     if (workspace_bytes < need)
         return fail(MSA_ERR_WORKSPACE, "msa_select_prefill: workspace of %zu bytes, %zu needed", workspace_bytes,
@@ -185,8 +197,47 @@ msa_status_t msa_select_prefill(const void *q_idx, const void *kidx_cache, const
     uint64_t *lists = static_cast<uint64_t *>(workspace);
     cudaError_t e = launch_score_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s,
                                          nullptr, lists, err_word, cs);
-    if (e == cudaSuccess) e = launch_topk_merge(lists, q_pos, n_rows, s, n_chunks, sel, err_word, cs);
+    if (e == cudaSuccess) e = launch_topk_merge(lists, q_pos, n_rows, s, n_chunks, sel, InvMark{}, err_word, cs);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_select_prefill");
+}
+
+msa_status_t msa_select_invert_prefill(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
+                                       const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
+                                       int32_t n_pages, const msa_dims_t *dims, int32_t *sel, int32_t *blk_off,
+                                       int32_t *blk_ent, int32_t *ent_pos, void *workspace, size_t workspace_bytes,
+                                       int32_t *err_word, msa_stream_t stream) {
+    Shape s;
+    msa_status_t st = check_select_prefill(dims, &s, "msa_select_invert_prefill");
+    if (st != MSA_OK) return st;
+    MSA_REQUIRE(n_rows >= 0 && n_req > 0 && n_pages > 0, "msa_select_invert_prefill: bad sizes");
+    MSA_REQUIRE(blk_off && err_word, "msa_select_invert_prefill: NULL pointer");
+    MSA_REQUIRE(n_rows == 0 || (q_idx && kidx_cache && block_table && q_req && q_pos && sel && blk_ent && ent_pos),
+                "msa_select_invert_prefill: NULL pointer");
+    if (1.0 * n_rows * s.G * s.topk > 2147483647.0)
+        return fail(MSA_ERR_UNSUPPORTED, "msa_select_invert_prefill: more than 2^31 entries");
+    MSA_REQUIRE(workspace, "msa_select_invert_prefill: NULL workspace");
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u)
+        return fail(MSA_ERR_INVALID_ARG, "msa_select_invert_prefill: workspace must be 16-byte aligned");
+    const size_t lists_bytes = select_lists_bytes(n_rows, s);
+    const size_t need = lists_bytes + invert_workspace_bytes(n_rows, n_req, s);
+    if (workspace_bytes < need)
+        return fail(MSA_ERR_WORKSPACE, "msa_select_invert_prefill: workspace of %zu bytes, %zu needed",
+                    workspace_bytes, need);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    void *inv_ws = static_cast<uint8_t *>(workspace) + lists_bytes;
+    cudaError_t e;
+    const InvMark mark = invert_clear(q_req, n_rows, n_req, s, inv_ws, cs, &e);
+    if (e == cudaSuccess && n_rows > 0) {
+        uint64_t *lists = static_cast<uint64_t *>(workspace);
+        e = launch_score_prefill(q_idx, kidx_cache, block_table, q_req, q_pos, n_rows, n_req, n_pages, s, nullptr,
+                                 lists, err_word, cs);
+        if (e == cudaSuccess)
+            e = launch_topk_merge(lists, q_pos, n_rows, s, score_prefill_chunks(s.max_blocks), sel, mark, err_word,
+                                  cs);
+    }
+    if (e == cudaSuccess)
+        e = launch_invert_finish(sel, q_req, n_rows, n_req, s, blk_off, blk_ent, ent_pos, inv_ws, err_word, cs);
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_select_invert_prefill");
 }
 
 msa_status_t msa_topk_blocks(const float *scores, const int32_t *q_pos, int32_t n_rows, const msa_dims_t *dims,
@@ -382,6 +433,10 @@ size_t msa_workspace_bytes(int32_t op, int32_t n_rows, int32_t n_req, const msa_
     if (op == MSA_OP_SELECT_PREFILL) {
         if (check_dims(dims, false, true, &s, "msa_workspace_bytes") != MSA_OK) return 0;
         return size_t(n_rows) * s.G * score_prefill_chunks(s.max_blocks) * kSelectListLen * sizeof(uint64_t);
+    }
+    if (op == MSA_OP_SELECT_INVERT_PREFILL) {
+        if (check_dims(dims, false, true, &s, "msa_workspace_bytes") != MSA_OK || n_req <= 0) return 0;
+        return select_lists_bytes(n_rows, s) + invert_workspace_bytes(n_rows, n_req, s);
     }
     return 0;
 }

@@ -56,8 +56,16 @@ cudaError_t launch_score_prefill(const void *q_idx, const void *kidx, const int3
 // candidates kept per list, and the merge of the lists into the selection.
 int score_prefill_chunks(int max_blocks);
 constexpr int kSelectListLen = 15;
+// Target of the inversion's first pass (bit q of key k at bitmap[k * words + q / 32]);
+// bitmap == nullptr means "do not mark".
+struct InvMark {
+    uint32_t *bitmap;
+    size_t words;
+    const int32_t *q_req;
+    int n_req;
+};
 cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n_rows, const Shape &s,
-                              int n_chunks, int32_t *sel, int32_t *err, cudaStream_t st);
+                              int n_chunks, int32_t *sel, const InvMark &mark, int32_t *err, cudaStream_t st);
 
 cudaError_t launch_topk(const float *scores, const int32_t *q_pos, int n_rows, const Shape &s,
                         int32_t *sel, int32_t *err, cudaStream_t st);
@@ -70,6 +78,14 @@ size_t invert_workspace_bytes(int n_rows, int n_req, const Shape &s);
 cudaError_t launch_invert(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req,
                           const Shape &s, int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws,
                           int32_t *err, cudaStream_t st);
+// The inversion in two halves around a caller that marks the bitmap itself:
+// invert_clear zeroes the bitmap in the inversion workspace and returns the mark
+// target; launch_invert_finish counts, scans and emits from the marked bitmap.
+InvMark invert_clear(const int32_t *q_req, int n_rows, int n_req, const Shape &s, void *ws, cudaStream_t st,
+                     cudaError_t *e);
+cudaError_t launch_invert_finish(const int32_t *sel, const int32_t *q_req, int n_rows, int n_req, const Shape &s,
+                                 int32_t *blk_off, int32_t *blk_ent, int32_t *ent_pos, void *ws, int32_t *err,
+                                 cudaStream_t st);
 
 // Block-major prefill attention: a plan kernel writes the chunk work list into
 // the workspace, then one persistent CTA per SM consumes it.

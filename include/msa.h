@@ -89,6 +89,7 @@ typedef void *msa_stream_t;
 #define MSA_OP_DECODE  1
 #define MSA_OP_PREFILL 2
 #define MSA_OP_SELECT_PREFILL 3
+#define MSA_OP_SELECT_INVERT_PREFILL 4
 
 /*
  * msa_index_score -- block scores for every (row, group, candidate block).
@@ -145,6 +146,28 @@ msa_status_t msa_select_prefill(const void *q_idx, const void *kidx_cache, const
                                 const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
                                 int32_t n_pages, const msa_dims_t *dims, int32_t *sel, void *workspace,
                                 size_t workspace_bytes, int32_t *err_word, msa_stream_t stream);
+
+/*
+ * msa_select_invert_prefill -- msa_select_prefill followed by
+ * msa_invert_selection, with the same outputs as those two calls.  [T-zh 未来工作]:
+ * the top-k kernel and the q-kv -> kv-q remap kernel are fusion candidates; here
+ * the kernel that merges the candidate lists into the selection also marks each
+ * selected (key, row) for the inversion, so the remap's first pass needs no
+ * kernel of its own.
+ *
+ *   q_idx ... dims        as msa_select_prefill
+ *   sel                   int32 [n_rows][G][topk]  out, as msa_select_prefill
+ *   blk_off, blk_ent, ent_pos  out, as msa_invert_selection
+ *   workspace  device scratch of msa_workspace_bytes(MSA_OP_SELECT_INVERT_PREFILL,
+ *              n_rows, n_req, dims) bytes, 16-byte aligned (candidate lists, then
+ *              the inversion's workspace)
+ * Limits: those of msa_select_prefill and msa_invert_selection.
+ */
+msa_status_t msa_select_invert_prefill(const void *q_idx, const void *kidx_cache, const int32_t *block_table,
+                                       const int32_t *q_req, const int32_t *q_pos, int32_t n_rows, int32_t n_req,
+                                       int32_t n_pages, const msa_dims_t *dims, int32_t *sel, int32_t *blk_off,
+                                       int32_t *blk_ent, int32_t *ent_pos, void *workspace, size_t workspace_bytes,
+                                       int32_t *err_word, msa_stream_t stream);
 
 /*
  * msa_topk_blocks -- per (row, group): the own block q_pos/128 is always kept;

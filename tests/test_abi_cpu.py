@@ -109,6 +109,10 @@ def test_workspace_sizes_and_errors(lib):
     assert lib.msa_workspace_bytes(9, 8, 1, ctypes.byref(d)) == 0
     # prefill work list: 16-byte header + one {key, first tile} pair per chunk of <= 8 tiles,
     # at most one partial chunk per key plus the entries split into full chunks of 8 x 16 entries
+    # fused selection + inversion: the candidate lists (one list of 15 keys per 128-block chunk),
+    # 256-byte rounded, then the inversion's workspace
+    sel_inv = lib.msa_workspace_bytes(4, 8192, 1, ctypes.byref(d))
+    assert sel_inv == ((8192 * 8 * 5 * 15 * 8 + 255) // 256) * 256 + inv
     pre = lib.msa_workspace_bytes(2, 8192, 1, ctypes.byref(d))
     assert pre == 16 + 8 * (8 * 533 + (8192 * 8 * 16 + 127) // 128)
     rc = lib.msa_sparse_attn_prefill(*([FAKE] * 8), 8192, 1, 4096, ctypes.byref(d), FAKE, FAKE, FAKE,

@@ -117,8 +117,9 @@ def _fused_cases():
 
 @pytest.mark.parametrize("name,make", list(_fused_cases()), ids=[n for n, _ in _fused_cases()])
 def test_fused_select_equals_score_then_topk(msa, name, make):
-    """msa_select_prefill (top-k fused into scoring) selects exactly what msa_index_score +
-    msa_topk_blocks select, so the whole prefill step gives identical bits."""
+    """msa_select_invert_prefill (top-k fused into scoring, the inversion's marks into
+    the list merge) selects and inverts exactly what msa_index_score + msa_topk_blocks +
+    msa_invert_selection do, so the whole prefill step gives identical bits."""
     case = make()
     unfused = _run(msa, case, fuse_topk=False)
     fused = _run(msa, case, fuse_topk=True)
@@ -127,8 +128,13 @@ def test_fused_select_equals_score_then_topk(msa, name, make):
     n_ent = int(unfused.blk_off[-1])        # entries past the CSR's end are scratch
     assert torch.equal(fused.blk_off, unfused.blk_off)
     assert torch.equal(fused.blk_ent[:n_ent], unfused.blk_ent[:n_ent])
+    assert torch.equal(fused.ent_pos, unfused.ent_pos)
     assert torch.equal(fused.out, unfused.out)
     assert torch.equal(fused.lse, unfused.lse)
+    # msa_select_prefill alone (no inversion) selects the same
+    d = msa.dims_of(case)
+    sel = msa.msa_select_prefill(case.q_idx, case.kidx_cache, case.block_table, case.q_req, case.q_pos, d)
+    assert torch.equal(sel, unfused.sel)
 
 
 def test_topk_bit_exact_on_oracle_scores(msa):
