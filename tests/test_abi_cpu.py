@@ -107,12 +107,18 @@ def test_workspace_sizes_and_errors(lib):
     assert dec == (((8 * 8 * 16 * 8 * 128 * 4 + 255) // 256) * 256 + ((8 * 8 * 16 * 8 * 4 + 255) // 256) * 256
                    + ((8 * 8 * 4 + 255) // 256) * 256)
     assert lib.msa_workspace_bytes(9, 8, 1, ctypes.byref(d)) == 0
-    # prefill work list: 16-byte header + one {key, first tile} pair per chunk of <= 8 tiles,
-    # at most one partial chunk per key plus the entries split into full chunks of 8 x 16 entries
     # fused selection + inversion: the candidate lists (one list of 15 keys per 128-block chunk),
     # 256-byte rounded, then the inversion's workspace
     sel_inv = lib.msa_workspace_bytes(4, 8192, 1, ctypes.byref(d))
     assert sel_inv == ((8192 * 8 * 5 * 15 * 8 + 255) // 256) * 256 + inv
+    # ... refused before any launch when too small, misaligned, or for topk > 16
+    sel_args = lambda dims, ws, nbytes: (*([FAKE] * 5), 8192, 1, 4096, ctypes.byref(dims), *([FAKE] * 4), ws,
+                                         ctypes.c_size_t(nbytes), FAKE, None)
+    assert lib.msa_select_invert_prefill(*sel_args(d, FAKE, sel_inv - 1)) == 6
+    assert lib.msa_select_invert_prefill(*sel_args(d, ctypes.c_void_p(0x1008), sel_inv)) == 1
+    assert lib.msa_select_invert_prefill(*sel_args(good_dims(max_blocks=533, topk=17), FAKE, 1 << 40)) == 2
+    # prefill work list: 16-byte header + one {key, first tile} pair per chunk of <= 8 tiles,
+    # at most one partial chunk per key plus the entries split into full chunks of 8 x 16 entries
     pre = lib.msa_workspace_bytes(2, 8192, 1, ctypes.byref(d))
     assert pre == 16 + 8 * (8 * 533 + (8192 * 8 * 16 + 127) // 128)
     rc = lib.msa_sparse_attn_prefill(*([FAKE] * 8), 8192, 1, 4096, ctypes.byref(d), FAKE, FAKE, FAKE,
