@@ -34,7 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch, from one-pass ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels on the
 # bench workloads; None when no capture of the current kernel exists.
-NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2775850000}
+NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2776050000}
 
 
 def parse_args():

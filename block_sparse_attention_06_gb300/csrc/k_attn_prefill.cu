@@ -622,26 +622,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
 
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_full[wg], k & 1, err, &sm.abort))) break;
             tc_fence_after();
-            // pass 1: row max over the visible tokens (32-column chunks; loops kept rolled so the
-            // code stays small enough for the instruction cache of a 16-warp CTA)
+            // pass 1: row max over the visible tokens, two 32-column TMEM loads per wait (half the
+            // load round trips; the loops stay rolled so the code stays small enough for the
+            // instruction cache of a 19-warp CTA -- unrolling pass 2 the same way was slower)
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll 1
-            for (int c = 0; c < 128; c += 32) {
-                uint32_t v[32];
-                tmem_ld32(t_s + uint32_t(c), v);
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                uint32_t vv[2][32];
+                tmem_ld32(t_s + uint32_t(c0), vv[0]);
+                tmem_ld32(t_s + uint32_t(c0 + 32), vv[1]);
                 tmem_ld_wait();
-                if (c + 31 <= lim) {   // fully visible chunk (every block but a row's own one)
 #pragma unroll
-                    for (int i = 0; i < 32; i += 16)
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int c = c0 + 32 * hh;
+                    const uint32_t(&v)[32] = vv[hh];
+                    if (c + 31 <= lim) {   // fully visible chunk (every block but a row's own one)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            mx[j] = fmax3(mx[j], __uint_as_float(v[i + j]), __uint_as_float(v[i + 8 + j]));
-                } else {
+                        for (int i = 0; i < 32; i += 16)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                            for (int j = 0; j < 8; ++j)
+                                mx[j] = fmax3(mx[j], __uint_as_float(v[i + j]), __uint_as_float(v[i + 8 + j]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            mx[i & 7] = fmaxf(mx[i & 7], (c + i <= lim) ? __uint_as_float(v[i]) : -INFINITY);
+                    }
                 }
             }
             const float m = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
