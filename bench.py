@@ -190,7 +190,7 @@ def run_msa(args, rank, world, local):
         line.update(dec)
         line["decode_multi"] = bench_decode_multi(args, world, dev, peaks, peak_src)
     if args.only in ("all", "prefill"):
-        line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src)
+        line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src, rank)
     line["clocks"] = clocks.stop()
     if case is not None:
         line["cpu_baseline"] = (cpu_baseline_decode(rank, case=case)
@@ -201,7 +201,7 @@ def run_msa(args, rank, world, local):
                 "warmup": W, "ms_per_step": pre["ms_per_step"], "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
                 "config": pre["config"], "gpu_launches": pre["gpu_launches"], "roofline": pre["roofline"],
-                "clocks": line["clocks"]}
+                "clocks": line["clocks"], "cpu_baseline": pre.get("cpu_baseline")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -344,7 +344,7 @@ def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
     }
 
 
-def bench_prefill(args, world, dev, peaks, peak_src):
+def bench_prefill(args, world, dev, peaks, peak_src, rank=0):
     import torch
     import block_sparse_attention_06_gb300 as msa
     import msa_inputs as mi
@@ -397,6 +397,8 @@ def bench_prefill(args, world, dev, peaks, peak_src):
                      "flops_per_launch": flops, "ms_per_launch": attn_ms,
                      "peak_source": f"{peak_src} bf16_tflops (burst)"},
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        prefill["cpu_baseline"] = cpu_baseline_prefill(pc)
     return prefill
 
 
@@ -427,6 +429,39 @@ def _oracle_decode_one(case, b):
     pt, rl = oracle.page_table(sel, bt_a, q_pos + 1)
     oracle.paged_attention(case.q[b:b + 1].cpu(), kc, vc, pt, rl, case.dims.sm_scale)
     return t_sel + time.perf_counter() - t
+
+
+def cpu_baseline_prefill(pc, budget_s: float = 10.0, max_rows: int = 2048):
+    """The fp64 oracle's prefill of single rows of the chunk -- scores against the row's
+    candidate blocks, top-k, attention over the selected tokens -- on host copies of the
+    chunk's pages, over rows spread through the chunk, until budget_s of CPU time."""
+    import torch
+    import oracle
+    bt = pc.block_table.cpu()
+    pages = torch.unique(bt[bt >= 0]).long()
+    local = torch.full((int(pages.max()) + 1,), -1, dtype=torch.int32)
+    local[pages] = torch.arange(len(pages), dtype=torch.int32)
+    bt_l = torch.where(bt >= 0, local[bt.clamp(min=0).long()], torch.full_like(bt, -1))
+    dev_pages = pages.to(pc.kidx_cache.device)
+    kidx, kc, vc = pc.kidx_cache[dev_pages].cpu(), pc.k_cache[dev_pages].cpu(), pc.v_cache[dev_pages].cpu()
+    q_idx, q, q_pos, q_req = pc.q_idx.cpu(), pc.q.cpu(), pc.q_pos.cpu(), pc.q_req.cpu()
+    zero = torch.zeros(1, dtype=torch.int32)
+    spent, done = 0.0, 0
+    for i in range(max_rows):
+        r = (i * 2654435761) % pc.n_rows      # rows spread over the chunk, every row position alike
+        b = int(q_req[r])
+        t = time.perf_counter()
+        sc = oracle.block_scores(q_idx[r:r + 1], kidx, bt_l[b:b + 1], zero, q_pos[r:r + 1], pc.max_blocks)
+        sel = oracle.topk(sc, q_pos[r:r + 1], pc.dims.topk)
+        oracle.attention(q[r:r + 1], kc, vc, bt_l[b:b + 1], zero, q_pos[r:r + 1], sel, pc.dims.sm_scale)
+        spent += time.perf_counter() - t
+        done += 1
+        if spent >= budget_s:
+            break
+    return {"value": done / spent, "unit": "q-tok/s", "cores": 1, "kind": "oracle", "host_cores": os.cpu_count(),
+            "sample": f"{done} rows spread over the {pc.n_rows}-row chunk, each scored against its candidate "
+                      f"blocks, selected and attended by the single-threaded fp64 C oracle, {spent:.1f} s of "
+                      f"CPU time"}
 
 
 def cpu_baseline_decode(rank: int, budget_s: float = 12.0, max_reqs: int = 1000, case=None):
