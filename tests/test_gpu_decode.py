@@ -88,6 +88,15 @@ def test_decode_shape_variants(msa, hq, g, d, di):
     _check_decode(msa, case)
 
 
+@pytest.mark.parametrize("topk", [1, 32])
+def test_decode_topk_limits(msa, topk):
+    """topk = 1 (the own block alone) and topk = 32 (the largest supported): rows with
+    fewer candidates than topk, exactly topk, and many more."""
+    case = mi.decode_case([100, 129, 32 * 128, 32 * 128 + 1, 20000], Hq=16, G=2, D=128, Di=64, topk=topk,
+                          pool_pages=300, needles_per_group=2, seed=17, device=DEV)
+    _check_decode(msa, case)
+
+
 def test_decode60k_full(msa):
     case = mi.named_case("decode60k", device=DEV)
     _check_decode(msa, case)

@@ -94,6 +94,19 @@ def test_prefill_shape_variants(msa, hq, g, d, di):
     _check_prefill(msa, case)
 
 
+@pytest.mark.parametrize("topk", [1, 32])
+def test_prefill_topk_limits(msa, topk):
+    """topk = 1 (each row attends its own block only) and topk = 32 (the largest
+    supported, past the fused selection's limit of 16): 300 rows from position 3,900,
+    so early rows have fewer than 32 candidates and later ones more."""
+    case = mi.prefill_case(3900, 300, Hq=16, G=2, D=128, Di=64, topk=topk, pool_pages=60, seed=14, device=DEV)
+    _check_prefill(msa, case)
+    fused = _run(msa, case, fuse_topk=None)   # the default path PrefillStep picks for this topk
+    unfused = _run(msa, case, fuse_topk=False)
+    assert fused.fuse_topk == (topk <= 16)
+    assert torch.equal(fused.out, unfused.out) and torch.equal(fused.lse, unfused.lse)
+
+
 def test_prefill68k_sampled(msa):
     """8192-row chunk on a 60,000-token prefix, full launch; oracle on sampled rows
     (first/last tile, a span boundary, the ragged positions around block edges)."""
