@@ -34,7 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch, from one-pass ncu captures
 # (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels on the
 # bench workloads; None when no capture of the current kernel exists.
-NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2776050000}
+NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2776050000, "k_score_decode_mt": 495690000}
 
 
 def parse_args():
@@ -339,7 +339,8 @@ def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
         "config": {"workload": f"decode60k with {T} query rows per request", "batch": 8, "rows": case.n_rows,
                    "ctx": 60000, "G": dims.G, "Di": dims.Di},
         "roofline": {"bound": "hbm", "kernel": "k_score_decode_mt", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None, "bytes_per_launch": kbytes,
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC["k_score_decode_mt"],
+                     "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} hbm_gbs"},
     }
 
