@@ -390,7 +390,8 @@ def bench_prefill(args, world, dev, peaks, peak_src, rank=0):
         "unit": "q-tok/s", "ms_per_step": pre_ms / K, "steps": K,
         "config": {"workload": "prefill68k" if pc.name == "prefill68k" else "prefill",
                    "prefix": args.prefill_prefix, "chunk": pc.n_rows, "Hq": pd.Hq, "G": pd.G,
-                   "D": pd.D, "Di": pd.Di, "topk": pd.topk},
+                   "D": pd.D, "Di": pd.Di, "topk": pd.topk,
+                   "l2": "working set larger than L2 (about 2.1 GB of partials written and read per step)"},
         "gpu_launches": ps.kernel_launches * K,
         "roofline": {"bound": "tensor", "kernel": "k_attn_prefill", "achieved": tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
