@@ -59,8 +59,9 @@ __device__ __forceinline__ uint32_t swz_off(int t, int c) {
 // r*topk + slot, are cut into gridDim.x contiguous ranges, one per CTA and one CTA
 // per SM.  Inside its range a CTA keeps one online-softmax state per row segment
 // (the pages of one row that fall in the range), so it writes one partial per
-// segment -- one to three per row -- rather than one per page.  Warp 4 (lane 0)
-// streams the range's K and V pages through an NS-deep ring of shared-memory
+// segment rather than one per page: at most 1 + ceil(topk / shortest range) per
+// row, e.g. four for 16 pages per row over ranges of 6 or 7 pages.  Warp 4 (lane
+// 0) streams the range's K and V pages through an NS-deep ring of shared-memory
 // stages with TMA while warps 0-3 attend: loads of later pages stay in flight
 // during the compute of the current one.
 template <int D, int HPG>
