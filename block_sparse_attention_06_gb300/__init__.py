@@ -141,6 +141,14 @@ def msa_check(err_word: torch.Tensor) -> None:
     _call("msa_check", _ptr(err_word), _stream(err_word.device))
 
 
+def msa_selftest_timeout(err_word: torch.Tensor) -> None:
+    """Queue the device self-test of the bounded-wait timeout: a wait that nothing
+    completes gives up after its limit (2 s) and raises MSA_FLAG_TIMEOUT in err_word,
+    which the next msa_check reports as MSA_ERR_TIMEOUT."""
+    _req(err_word, torch.int32, "err_word")
+    _call("msa_selftest_timeout", _ptr(err_word), _stream(err_word.device))
+
+
 def msa_workspace_bytes(op: int, n_rows: int, n_req: int, dims: Dims) -> int:
     d = dims.c()
     return int(_lib.msa_workspace_bytes(op, n_rows, n_req, ctypes.byref(d)))

@@ -475,4 +475,10 @@ const char *msa_last_error(void) { return g_last_error; }
 
 int32_t msa_version(void) { return 300; }
 
+msa_status_t msa_selftest_timeout(int32_t *err_word, msa_stream_t stream) {
+    MSA_REQUIRE(err_word, "msa_selftest_timeout: NULL err_word");
+    const cudaError_t e = launch_selftest_timeout(err_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_selftest_timeout");
+}
+
 }  // extern "C"

@@ -134,6 +134,9 @@ bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *di
 
 int sm_count();
 
+// One thread waits on an mbarrier that nothing arrives on (the device timeout path).
+cudaError_t launch_selftest_timeout(int32_t *err, cudaStream_t st);
+
 // Record the detail string that msa_last_error() returns on this thread.
 void set_last_error(const char *msg);
 

@@ -401,6 +401,17 @@ const char *msa_last_error(void);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t msa_version(void);
 
+/*
+ * msa_selftest_timeout -- exercises the device error path that every bounded
+ * wait of the library shares, without any fault: one thread waits on an
+ * mbarrier that nothing arrives on, gives up after the wait limit (2 s), raises
+ * MSA_FLAG_TIMEOUT in err_word and returns.  msa_check(err_word) then reports
+ * MSA_ERR_TIMEOUT and clears the word; the stream stays usable.
+ *
+ *   err_word  int32 device word, caller-owned
+ */
+msa_status_t msa_selftest_timeout(int32_t *err_word, msa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

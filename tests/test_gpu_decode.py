@@ -158,3 +158,16 @@ def test_packed_inputs_and_results(msa):
     torch.cuda.synchronize()
     msa.msa_check(step.err)
     assert torch.equal(h_out, ref_out) and torch.equal(h_lse, ref_lse)
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(msa):
+    """The device error path shared by every bounded wait: a wait that nothing completes
+    (msa_selftest_timeout) gives up after its limit, the host reads MSA_ERR_TIMEOUT, the
+    word is cleared, and the next decode step on the same stream runs clean."""
+    err = msa.new_err_word(DEV)
+    msa.msa_selftest_timeout(err)
+    with pytest.raises(msa.MsaError) as ei:
+        msa.msa_check(err)
+    assert ei.value.status == 5 and "TIMEOUT" in str(ei.value)
+    _, dec = mi.tiny_case(seed=1000, device=DEV)
+    _check_decode(msa, dec)
