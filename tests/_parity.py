@@ -10,6 +10,9 @@ Tolerances (fixed for the MSA hot path):
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+import os
+
 import numpy as np
 import torch
 
@@ -59,6 +62,60 @@ def assert_selection_where_unambiguous(gpu_sel, ref_sel, gap):
     diff = (g != r).any(dim=-1) & ok
     assert not bool(diff.any()), f"{int(diff.sum())} unambiguous (row, group) selections differ"
     return ok
+
+
+def assert_selection_valid(gpu_sel, ref_scores, q_pos, topk: int, page: int = 128):
+    """Every (row, group) selection -- near ties included -- is *a* correct top-k of the
+    oracle's scores within the score tolerance:
+
+      * k_eff = min(topk, own + 1) ids, strictly ascending, then -1 padding;
+      * every id is a candidate (0 .. own) and the last one is the own block;
+      * no dropped candidate beats a kept one by more than the two scores' tolerances:
+        min over kept non-own j of (s_j + tol_j) >= max over dropped i of (s_i - tol_i),
+        tol = 2e-3 * (|s| + 1) (the GPU scores are within that of the oracle's, so any
+        order the GPU can see between two blocks is one the oracle's values allow).
+    """
+    sel = gpu_sel.detach().cpu().numpy().astype(np.int64)
+    s = ref_scores.detach().cpu().double().numpy()
+    pos = q_pos.detach().cpu().numpy().astype(np.int64)
+    R, G, k = sel.shape
+    assert k == topk
+    own = pos // page
+    k_eff = np.minimum(topk, own + 1)
+    slot = np.arange(k)[None, None, :]
+    filled = np.broadcast_to(slot < k_eff[:, None, None], sel.shape)
+    assert np.all(sel[~filled] == -1), "padding slots past k_eff must be -1"
+    assert np.all(sel[filled] >= 0), "the first k_eff slots must hold block ids"
+    assert np.all(sel <= own[:, None, None]), "a selected block lies past the row's own block"
+    asc = np.diff(sel, axis=-1) > 0
+    need_asc = filled[..., 1:]
+    assert np.all(asc[need_asc]), "selected ids must be strictly ascending"
+    last = np.take_along_axis(sel, (k_eff - 1)[:, None, None].repeat(G, axis=1), axis=-1)[..., 0]
+    assert np.all(last == own[:, None]), "the own block must be selected (the last id)"
+    tol = SCORE_RTOL * (np.abs(s) + 1.0)
+    worst = 0.0
+    for r in range(R):
+        o = int(own[r])
+        if o + 1 <= topk or topk == 1:   # every candidate kept, or only the own block: nothing to rank
+            continue
+        for g in range(G):
+            kept = np.zeros(o, dtype=bool)
+            ids = sel[r, g, :k_eff[r]]
+            kept[ids[ids < o]] = True
+            lo = np.min(s[r, g, :o][kept] + tol[r, g, :o][kept])
+            hi = np.max(s[r, g, :o][~kept] - tol[r, g, :o][~kept])
+            worst = max(worst, hi - lo)
+    assert worst <= 0.0, f"a dropped block outranks a kept one by {worst:.3e} beyond the score tolerance"
+
+
+def assert_topk_of_own_scores(gpu_sel, gpu_scores, q_pos, topk: int):
+    """The GPU's selection is bit-exactly the oracle's top-k rule applied to the GPU's own
+    fp32 scores: near ties are then resolved exactly as the rule says (ties to the lower
+    block id), with nothing left to tolerance."""
+    want = oracle.topk(gpu_scores.detach().cpu().double(), q_pos.detach().cpu(), topk)
+    got = gpu_sel.detach().cpu()
+    bad = (got != want).any(dim=-1)
+    assert not bool(bad.any()), f"{int(bad.sum())} (row, group) selections differ from top-k of the GPU's scores"
 
 
 def assert_out(gpu_out, ref_out, what="out"):
@@ -149,3 +206,19 @@ def oracle_attention_on(case, rows, sel, block_table=None):
     vc = case.v_cache[pages.to(dev)].cpu()
     return oracle.attention(case.q.cpu()[idx], kc, vc, bt_c, local, case.q_pos.cpu()[idx], sel.cpu(),
                             case.dims.sm_scale)
+
+
+def in_row_chunks(fn, rows, *, threads=None, min_rows=8):
+    """Run fn(chunk_of_rows) -> tuple of tensors over row chunks in threads (the C oracle
+    releases the GIL) and concatenate the results along dim 0, in row order."""
+    rows = list(rows)
+    n = threads or min(16, os.cpu_count() or 1)
+    if len(rows) < 2 * min_rows or n <= 1:
+        return fn(rows)
+    step = max(min_rows, (len(rows) + n - 1) // n)
+    chunks = [rows[i:i + step] for i in range(0, len(rows), step)]
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        parts = list(ex.map(fn, chunks))
+    if isinstance(parts[0], tuple):
+        return tuple(torch.cat([p[i] for p in parts], dim=0) for i in range(len(parts[0])))
+    return torch.cat(parts, dim=0)

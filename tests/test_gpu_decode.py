@@ -55,6 +55,9 @@ def _check_decode(m, case, rows=None):
     gap = P.selection_gap(ref["scores"], q_pos, case.dims.topk)
     gsel = step.sel.cpu()[idx]
     P.assert_selection_where_unambiguous(gsel, ref["sel"], gap)
+    # near ties too: a valid top-k of the oracle's scores, and exactly the top-k of the GPU's own scores
+    P.assert_selection_valid(gsel, ref["scores"], q_pos, case.dims.topk)
+    P.assert_topk_of_own_scores(gsel, step.scores.cpu()[idx], q_pos, case.dims.topk)
     # page table + row lengths bit-exact for the GPU's own selection
     pt, rl = oracle.page_table(gsel, case.block_table.cpu()[case.q_req.cpu()[idx].long()], q_pos + 1)
     G = case.dims.G

@@ -1,11 +1,14 @@
 """K/V offload with the k-index kept on the GPU: the decode step reads K/V from
 page-locked host memory, gathering only the selected pages into a device pool
 (msa_offload_gather).  The result must equal the all-on-device step bit for bit:
-the same attention kernel runs on the same page contents, only the page ids differ."""
+the same attention kernel runs on the same page contents, only the page ids differ.
+It is also checked against the fp64 oracle, which reads K/V from the same host
+copies the offloaded step gathers from."""
 import pytest
 import torch
 
 import msa_inputs as mi
+import oracle
 from tests import _parity as P
 
 pytestmark = pytest.mark.gpu
@@ -44,6 +47,19 @@ def test_offloaded_decode_equals_device_decode(msa, lens, hq, g, d, di, topk):
         assert torch.equal(ppt < 0, ref.page_table < 0)
         assert torch.equal(out, out_ref)
         assert torch.equal(lse, lse_ref)
+    # against the oracle: scores and selection of the GPU-resident k-index, then attention over the
+    # GPU's selection with K/V taken from the host copies
+    rows = list(range(case.n_rows))
+    oref = P.oracle_decode_rows(case, rows)
+    q_pos = case.q_pos.cpu()
+    P.assert_scores(off.scores.cpu(), oref["scores"], q_pos)
+    P.assert_selection_valid(off.sel.cpu(), oref["scores"], q_pos, topk)
+    P.assert_topk_of_own_scores(off.sel.cpu(), off.scores.cpu(), q_pos, topk)
+    pages, bt_c = P.compact_pages(case.block_table.cpu(), off.sel.cpu(), case.q_req.cpu())
+    o_ref, l_ref = oracle.attention(case.q.cpu(), host_k[pages], host_v[pages], bt_c, case.q_req.cpu(), q_pos,
+                                    off.sel.cpu(), dims.sm_scale)
+    P.assert_out(out, o_ref, "offloaded out")
+    P.assert_lse(lse, l_ref, "offloaded lse")
     # the pool holds exactly the selected group slices
     pt = ref.page_table.cpu()
     for r in (0, case.n_rows * g - 1):
