@@ -34,9 +34,10 @@
 //              previous chunk's last S has completed, V_j once its last PV has;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
 //              from TMEM in 32-column chunks twice (row max, then exp2 and P as
-//              packed bf16 written over S); the row's 1/sum goes to shared
-//              memory and its lse to the partials; while one group runs its
-//              softmax the tensor core works on the other group's tile;
+//              packed bf16 written over S); the row's 1/sum goes to a four-slot
+//              ring in shared memory (so a group never waits for the epilogue to
+//              read the previous one) and its lse to the partials; while one group
+//              runs its softmax the tensor core works on the other group's tile;
 //   warps 12-15  epilogue: every tile in order, O chunk by chunk from TMEM,
 //              normalised, into the shared staging buffer in the 128B-swizzled
 //              box layout, so a softmax group goes on to its next tile as soon
@@ -46,11 +47,16 @@
 //              no warp waits for another to reuse the staging buffer;
 //   warp 17    idle (it would share the MMA warp's sub-partition);
 //   warps 16, 3, 18  Q loaders, one per Q buffer, one tile each in turn: the HPG
-//              heads of each entry's query row (HPG * D * 2 contiguous bytes) by
-//              16-byte cp.async, in the 128B-swizzled layout the MMA reads.  One
-//              instruction moves 512 contiguous bytes, where a TMA box of the
-//              swizzled layout can move only 8 rows of 128 bytes.  A buffer has
-//              one loader, so its barriers' phases are waited in order.
+//              heads of each entry's query row (HPG * D * 2 contiguous bytes) in
+//              the 128B-swizzled layout the MMA reads.  With HPG = 8 an entry's
+//              heads fill whole 1024-byte swizzle atoms, so one TMA box of 64
+//              columns x 8 heads per entry and sub-tile moves them (a query row of
+//              -1, padding, reads the zero fill): 16 instructions of one lane per
+//              tile instead of 512 cp.async, which leaves the loaders' issue slots
+//              to the softmax and epilogue warps on their sub-partitions.  With
+//              HPG = 4 a box would cover half an atom, so the warp copies the rows
+//              by 16-byte cp.async.  A buffer has one loader, so its barriers'
+//              phases are waited in order.
 // TMEM: S0 | S1 | O0 | O1 (128 + 128 + D + D of 512 columns).
 // Every wait is bounded; a timeout raises MSA_FLAG_TIMEOUT and every role drains.
 #include "msa_device.cuh"
@@ -88,12 +94,12 @@ struct AttnSmem {
     alignas(1024) uint8_t q[kQBuf][128 * D * 2];
     alignas(1024) uint8_t stg[128 * D * 2];         // one tile's bf16 output on its way to the partials
     TileDesc desc[kRing];
-    float inv_le[2][128];                           // 1 / row sum of P, per S/O buffer (softmax -> epilogue)
+    float inv_le[4][128];                           // 1 / row sum of P, per tile mod 4 (softmax -> epilogue)
     int32_t chunk_page[4], chunk_g[4];              // decoder -> K/V loader
     uint64_t k_full, k_empty, v_full, v_empty;
     uint64_t q_full[kQBuf], q_empty[kQBuf];
     uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
-    uint64_t stat_free[2];                          // inv_le[b] read by the epilogue
+    uint64_t stat_full[4], stat_free[4];            // inv_le[i] written / read by the epilogue
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
     uint64_t drain;
@@ -274,7 +280,7 @@ struct StoreMaps {
 
 template <int D, int HPG>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
-    const uint8_t *__restrict__ qg, int Hq, const __grid_constant__ CUtensorMap kmap,
+    const uint8_t *__restrict__ qg, int Hq, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ StoreMaps omaps,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos,
     const int32_t *__restrict__ blk_off, const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr,
@@ -303,10 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             mbar_init(&sm.p_full[b], 4);
             mbar_init(&sm.o_full[b], 1);
             mbar_init(&sm.o_free[b], 4);
-            mbar_init(&sm.stat_free[b], 4);
         }
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.v_empty, 1);
+        for (int r = 0; r < 4; ++r) {
+            mbar_init(&sm.stat_full[r], 4);
+            mbar_init(&sm.stat_free[r], 4);
+        }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(&sm.desc_ready[r], 32);
             mbar_init(&sm.desc_full[r], 1);   // the tile's Q loader, once it has read the descriptor
@@ -325,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
         for (int i = 0; i < kStoreBoxes; ++i) tma_prefetch_desc(&omaps.box[i]);
@@ -559,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         // this lane's chunks of an entry: head and chunk column of chunk j * 32 + lane
         const uint8_t *q_row0 = qg + size_t(lane % CPH) * 16;   // + head row offset below
         const int qb = warp == 16 ? 0 : warp == 3 ? 1 : 2;   // this warp's Q buffer: tiles u % kQBuf == qb
+        int n_tma = 0;   // tiles of this buffer whose Q boxes were issued
         for (int u = qb;; u += kQBuf) {
             const int slot = u % kRing;
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.desc_ready[slot], (u / kRing) & 1, err, &sm.abort))) break;
@@ -572,6 +583,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 !__all_sync(0xffffffffu, mbar_wait(&sm.q_empty[qb], ((u / kQBuf) - 1) & 1, err, &sm.abort)))
                 break;
             const int g = d.g;
+            if constexpr (HPG == 8) {
+                // one TMA box of 64 columns x 8 heads (one whole 1024-byte swizzle atom) per entry and
+                // sub-tile; a query row of -1 (padding, rejected entry) lies outside the tensor: zeros
+                const int qq = lane < EPT ? d.qq[lane] : -1;
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.desc_full[slot]);   // the descriptor has been read
+                    mbar_arrive_expect_tx(&sm.q_full[qb], 128 * D * 2);
+                }
+                __syncwarp();
+                if (lane < EPT) {
+#pragma unroll
+                    for (int i = 0; i < NSUB; ++i)
+                        tma_load_3d(sm.q[qb] + i * 16384 + lane * (HPG * 128), &qmap, &sm.q_full[qb], i * 64,
+                                    g * HPG, qq);
+                }
+                ++n_tma;
+                continue;
+            }
             const uint32_t qdst = smem_u32(sm.q[qb]);
 #pragma unroll 1
             for (int e = 0; e < EPT; ++e) {
@@ -599,6 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             if (lane == 0) mbar_arrive(&sm.q_full[qb]);
         }
         cp_async_wait<0>();   // nothing in flight when the CTA exits
+        // on abort, this buffer's last Q boxes land before the CTA exits (its earlier phases completed)
+        if (n_tma > 0 && sm.abort && lane == 0) mbar_wait(&sm.q_full[qb], (n_tma - 1) & 1, err, nullptr);
     } else if (warp < 12) {
         // ------------------------------------------------------------ softmax groups (warps 4-11)
         const int wg = (warp - 4) >> 2;
@@ -608,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
         const uint32_t t_s = tmem + lane_off + uint32_t(wg * 128);
         const float scale = sm_scale * kLog2e;
+        const uint64_t scale2 = dup2(scale);
         for (int u = wg;; u += 2) {
             const int slot = u % kRing;
             const int k = u >> 1;
@@ -653,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             }
             const float m = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             const float ms = m * scale;
-            const uint64_t scale2 = dup2(scale), nms2 = dup2(-ms);
+            const uint64_t nms2 = dup2(-ms);
             // pass 2: probabilities 2^(s*scale - ms) as packed bf16 over the columns already read
             // (P of chunk c lands in columns c/2 .. c/2+15, below the chunks still to read); their
             // fp32 sum in eight chains (four lane pairs) normalises O and gives the lse
@@ -688,15 +721,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 tmem_st16(t_s + uint32_t(c >> 1), w);
             }
             const float le = (sum2(acc2[0]) + sum2(acc2[1])) + (sum2(acc2[2]) + sum2(acc2[3]));
-            // inv_le[wg] is free once the epilogue has read it for this group's previous tile
-            if (k >= 1 && !__all_sync(0xffffffffu, mbar_wait(&sm.stat_free[wg], (k - 1) & 1, err, &sm.abort)))
+            // slot u % 4 is free once the epilogue has read tile u - 4's row sums
+            if (u >= 4 && !__all_sync(0xffffffffu, mbar_wait(&sm.stat_free[u & 3], ((u >> 2) - 1) & 1, err, &sm.abort)))
                 break;
-            sm.inv_le[wg][row] = 1.0f / le;
+            sm.inv_le[u & 3][row] = 1.0f / le;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[wg]);
-            if (qq >= 0) lse_part[size_t(idx) * HPG + h] = (ms + log2f(le)) * kLn2;
+            if (lane == 0) {
+                mbar_arrive(&sm.stat_full[u & 3]);
+                mbar_arrive(&sm.p_full[wg]);
+            }
+            float lg;
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(le));
+            if (qq >= 0) lse_part[size_t(idx) * HPG + h] = (ms + lg) * kLn2;
         }
     } else {
         // ------------------------------------------------------------ epilogue (warps 12-15)
@@ -717,11 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const int b = u & 1, k = u >> 1;
             const uint32_t t_o = tmem + lane_off + uint32_t(256 + b * D);
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.o_full[b], k & 1, err, &sm.abort))) break;
-            // P (and with it inv_le) of tile u is complete: this wait orders the read below
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.p_full[b], k & 1, err, &sm.abort))) break;
-            const uint64_t inv2 = dup2(sm.inv_le[b][row]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.stat_full[u & 3], (u >> 2) & 1, err, &sm.abort))) break;
+            const uint64_t inv2 = dup2(sm.inv_le[u & 3][row]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.stat_free[b]);
+            if (lane == 0) mbar_arrive(&sm.stat_free[u & 3]);
             // this warp's 32 staging rows are free once its stores of tile u - 1 have read them
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -800,9 +837,15 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
                      const int32_t *q_pos, const int32_t *blk_off, const int32_t *blk_ent, int n_rows, int n_req,
                      int n_pages, const Shape &s, void *o_part, float *lse_part, void *ws, int32_t *err,
                      cudaStream_t st) {
-    alignas(64) CUtensorMap km, vm;
+    alignas(64) CUtensorMap qm, km, vm;
     alignas(64) StoreMaps om;
     const char *why = nullptr;
+    {
+        const uint64_t dims[3] = {uint64_t(D), uint64_t(s.Hq), uint64_t(n_rows)};
+        const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(s.Hq) * D * 2};
+        const uint32_t box[3] = {64u, uint32_t(HPG), 1u};
+        if (!encode_tensor_map(&qm, 3, q, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
+    }
     {
         const uint64_t dims[4] = {uint64_t(D), uint64_t(s.G), 128ull, uint64_t(n_pages)};
         const uint64_t strides[3] = {uint64_t(D) * 2, uint64_t(s.G) * D * 2, 128ull * s.G * D * 2};
@@ -831,7 +874,7 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
     e = cudaFuncSetAttribute(k_attn_prefill<D, HPG>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true,
-                         static_cast<const uint8_t *>(q), s.Hq, km,
+                         static_cast<const uint8_t *>(q), s.Hq, qm, km,
                          vm, om, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows,
                          n_req, n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, lse_part, err);
 }

@@ -36,13 +36,23 @@ def _check_prefill(m, case, rows=None, check_partials=True):
     q_pos, q_req = case.q_pos.cpu()[idx], case.q_req.cpu()[idx]
     bt = case.block_table.cpu()
     local_bt = bt[q_req.long()]
-    local = torch.arange(len(rows), dtype=torch.int32)
-    ref_sc = oracle.block_scores(case.q_idx.cpu()[idx], case.kidx_cache.cpu(), local_bt, local, q_pos, case.max_blocks)
+    kidx = case.kidx_cache.cpu()
+    q_idx = case.q_idx.cpu()
+
+    def scores_of(chunk):   # chunk: positions into `rows`
+        ci = torch.as_tensor(chunk)
+        return oracle.block_scores(q_idx[idx[ci]], kidx, local_bt[ci], torch.arange(len(chunk), dtype=torch.int32),
+                                   q_pos[ci], case.max_blocks)
+
+    ref_sc = P.in_row_chunks(scores_of, range(len(rows)))
     P.assert_scores(step.scores.cpu()[idx], ref_sc, q_pos)
     ref_sel = oracle.topk(ref_sc, q_pos, case.dims.topk)
     gap = P.selection_gap(ref_sc, q_pos, case.dims.topk)
     gsel = step.sel.cpu()[idx]
     P.assert_selection_where_unambiguous(gsel, ref_sel, gap)
+    # near ties too: a valid top-k of the oracle's scores, and exactly the top-k of the GPU's own scores
+    P.assert_selection_valid(gsel, ref_sc, q_pos, case.dims.topk)
+    P.assert_topk_of_own_scores(gsel, step.scores.cpu()[idx], q_pos, case.dims.topk)
     # inversion of the GPU's full selection is bit-exact, and ent_pos is its inverse
     off, ent = oracle.invert(step.sel.cpu(), case.q_req.cpu(), case.n_req, case.max_blocks)
     assert torch.equal(step.blk_off.cpu(), off)
@@ -50,14 +60,21 @@ def _check_prefill(m, case, rows=None, check_partials=True):
     P.assert_ent_pos(step.sel.cpu(), step.ent_pos.cpu(), ent)
     # per-block partials (valid slots) and the merged output on the GPU's selection
     if check_partials:
-        kc, vc = case.k_cache.cpu(), case.v_cache.cpu()
-        op, lp = oracle.block_partials(case.q.cpu()[idx], kc, vc, local_bt, local, q_pos, gsel, case.dims.sm_scale)
+        kc, vc, qc = case.k_cache.cpu(), case.v_cache.cpu(), case.q.cpu()
+
+        def partials_of(chunk):
+            ci = torch.as_tensor(chunk)
+            return oracle.block_partials(qc[idx[ci]], kc, vc, local_bt[ci], torch.arange(len(chunk), dtype=torch.int32),
+                                         q_pos[ci], gsel[ci], case.dims.sm_scale)
+
+        op, lp = P.in_row_chunks(partials_of, range(len(rows)))
         hpg = case.dims.Hq // case.dims.G
         valid = (gsel >= 0).repeat_interleave(hpg, dim=1).transpose(1, 2)   # [rows][topk][Hq]
         o_by_slot, l_by_slot = step.partials_by_slot()
         P.assert_lse(l_by_slot[idx][valid], lp[valid], "lse_part")
         P.assert_out(o_by_slot[idx][valid], op[valid], "o_part")
-    o_ref, l_ref = P.oracle_attention_on(case, rows, gsel)
+    o_ref, l_ref = P.in_row_chunks(
+        lambda ch: P.oracle_attention_on(case, [rows[i] for i in ch], gsel[torch.as_tensor(ch)]), range(len(rows)))
     P.assert_out(step.out.cpu()[idx], o_ref)
     P.assert_lse(step.lse.cpu()[idx], l_ref)
     return step
@@ -107,11 +124,43 @@ def test_prefill_topk_limits(msa, topk):
     assert torch.equal(fused.out, unfused.out) and torch.equal(fused.lse, unfused.lse)
 
 
+def test_prefill_large_score_spread(msa):
+    """Peaky attention: keys of tokens 70 and 100 of every page scaled by -30 and 40, so a
+    row's scores inside one block spread over hundreds of units and one token takes nearly
+    all the weight (exp2 of very negative arguments, masked and unmasked chunks alike).  V is
+    scaled by 1/4: the output is then close to a single V row, and a row of N(0,1) values
+    rounded to bf16 twice (partial, merged output) can miss by 2^-8 of its magnitude, so the
+    smaller V keeps that rounding inside the absolute tolerance the test applies."""
+    case = mi.prefill_case(1000, 300, Hq=16, G=2, D=128, Di=64, topk=6, pool_pages=40, seed=12, device=DEV)
+    case.k_cache[:, 100] = (case.k_cache[:, 100].float() * 40).to(torch.bfloat16)
+    case.k_cache[:, 70] = (case.k_cache[:, 70].float() * -30).to(torch.bfloat16)
+    case.v_cache.mul_(0.25)
+    step = _check_prefill(msa, case)
+    # the spread is there: some row's score on token 100 lies more than 64 (log2 units) above zero
+    q = case.q.float().cpu()
+    k100 = case.k_cache[:, 100].float().cpu()                    # [pages][G][D]
+    hpg = case.dims.Hq // case.dims.G
+    s100 = torch.einsum("rgd,pgd->rgp", q.view(q.shape[0], case.dims.G, hpg, -1)[:, :, 0], k100)
+    assert float(s100.max()) * case.dims.sm_scale * 1.4427 > 64 + 10
+
+
 def test_prefill68k_sampled(msa):
-    """8192-row chunk on a 60,000-token prefix, full launch; oracle on sampled rows
-    (first/last tile, a span boundary, the ragged positions around block edges)."""
+    """8192-row chunk on a 60,000-token prefix, full launch; oracle on sampled rows: the
+    first and last row of every 128-row tile (the chunk starts at position 60,000, in the
+    middle of block 468, so tile edges and block edges differ), the rows around every
+    block edge inside the chunk, and a stride-37 sample through the whole chunk (471
+    rows) -- scores, selection, per-block partials, merged output and lse on each."""
     case = mi.named_case("prefill68k", device=DEV)
-    rows = [0, 1, 127, 128, 255, 256, 1000, 4095, 4096, 6000, 8190, 8191]
+    n = case.n_rows
+    first = int(case.q_pos[0])
+    rows = {0, n - 1}
+    for t in range(0, n, 128):                      # 128-row tile edges
+        rows.update((t, min(n - 1, t + 127)))
+    for p in range((first // 128 + 1) * 128, first + n, 128):   # block edges: last row of a block, first of the next
+        rows.update((p - first - 1, p - first))
+    rows.update(range(5, n, 37))                    # stride sample (every row position class alike)
+    rows = sorted(rows)
+    assert 400 <= len(rows) <= 520
     _check_prefill(msa, case, rows, check_partials=True)
 
 
