@@ -9,13 +9,25 @@
 // us a workspace.  This variant therefore keeps the segment partials in a
 // file-scope device array of fixed size instead of a caller-provided workspace.
 //
-// The array exists once per GPU that loads the library and stays allocated until
-// the process exits.  Every call uses the same array, so calls whose kernels
-// overlap on the GPU (for example on two streams) race on it and must be
-// serialised by the caller.  The array keeps what the previous call left in it.
-// Only the per-row merge counters have to start at zero, and
-// msa_sparse_attn_decode clears them on the stream before its kernel runs; the
-// partials and their lse are written before they are read.
+// The array exists once per GPU that uses the library and stays allocated until
+// the process exits.  With CUDA's lazy module loading (the default), the device
+// memory behind it is reserved when the library's module is first loaded on a
+// device, which is this entry point's first call there (the address lookup
+// below), not when the library is opened.  A caller that reserves nearly all HBM
+// for its own pool must therefore make that first call before it reserves the
+// pool; otherwise the lookup can fail for lack of memory, and the call returns
+// MSA_ERR_CUDA saying so.
+//
+// The address is looked up once per device and kept.  After cudaDeviceReset the
+// module is loaded again, possibly at another address, so a process that resets
+// a device must not call this entry point on it again.
+//
+// Every call uses the same array, so calls whose kernels overlap on the GPU (for
+// example on two streams) race on it and must be serialised by the caller.  The
+// array keeps what the previous call left in it.  Only the per-row merge
+// counters have to start at zero, and msa_sparse_attn_decode clears them on the
+// stream before its kernel runs; the partials and their lse are written before
+// they are read.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -79,8 +91,12 @@ msa_status_t msa_sparse_attn_decode_noalloc(const void *q, const void *k_cache, 
     void *scratch = nullptr;
     cudaError_t e = scratch_on_current_device(&scratch);
     if (e != cudaSuccess) {
-        char msg[256];
-        snprintf(msg, sizeof msg, "msa_sparse_attn_decode_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        char msg[384];
+        snprintf(msg, sizeof msg,
+                 "msa_sparse_attn_decode_noalloc: cudaGetSymbolAddress: %s (the first call on a device loads the "
+                 "library's module and its 16 MiB scratch array; make it before reserving the rest of device "
+                 "memory)",
+                 cudaGetErrorString(e));
         return fail(MSA_ERR_CUDA, msg);
     }
     return msa_sparse_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, dims, out, lse, scratch,

@@ -363,10 +363,15 @@ msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cac
  *   (for example B <= 31 requests at G = 8, topk = 16, Hq/G = 8, D = 128); larger
  *   calls return MSA_ERR_WORKSPACE and enqueue nothing.
  *   Allocation: none -- no cudaMalloc, cudaFree or allocating library routine.
- *   The array is static device memory that every GPU loading the library holds
- *   until the process exits.  The first call on a device looks up the array's
- *   device address (cudaGetSymbolAddress, with that device current); make that
- *   first call before any stream capture.
+ *   The array is static device memory that a GPU holds from the library's first
+ *   use on it until the process exits.  With CUDA's default lazy module loading
+ *   that first use is this entry point's first call on the device: it looks up
+ *   the array's device address (cudaGetSymbolAddress, with that device current),
+ *   which loads the module and reserves the 16 MiB.  Make that first call before
+ *   any stream capture and before reserving the rest of device memory for a KV
+ *   pool; if the reservation fails the call returns MSA_ERR_CUDA and says so.
+ *   The address is kept per device: do not call this entry point on a device
+ *   again after cudaDeviceReset.
  *   Sharing: all calls use the same array and find in it what the previous call
  *   left.  Calls whose kernels overlap on the GPU race on it, so the caller must
  *   serialise them (one stream, or events between streams).
