@@ -31,10 +31,10 @@ if ROOT not in sys.path:
 
 METRIC = "MSA decode tok/s & prefill q-tok/s at 60k ctx; % of HBM / tensor-core roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes (read + write) per launch, from one-pass ncu captures
-# (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels on the
-# bench workloads; None when no capture of the current kernel exists.
-NCU_TRAFFIC = {"k_score_decode": 495116800, "k_attn_prefill": 2776050000, "k_score_decode_mt": 495690000}
+PROFILES = os.path.join(ROOT, "profiles")
+CSRC = os.path.join(ROOT, "block_sparse_attention_06_gb300", "csrc")
+SWEEP = ("decode1m", "ragged1", "ragged8", "ragged32", "ragged64")
+L2_FLUSH_BYTES = 256 << 20   # written between timed steps of the small workloads (L2 is 129 MB)
 
 
 def parse_args():
@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--prefill-prefix", type=int, default=60000, help="cached tokens before the prefill chunk")
     ap.add_argument("--prefill-chunk", type=int, default=8192, help="new query rows in the prefill chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the decode1m and ragged-batch decode objects (profiling runs)")
     return ap.parse_args()
 
 
@@ -141,6 +143,30 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def ncu_traffic(kernel: str):
+    """DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of `kernel` on its bench
+    workload, from the machine-readable line of its ncu summary under profiles/:
+
+        <!-- traffic kernel=NAME source=FILE.cu sha256_16=HEX dram_bytes_per_launch=N -->
+
+    Reported only while the kernel's source is the one that was profiled (same sha256 prefix);
+    otherwise (traffic None, "stale ...") so that a changed kernel never carries old counters."""
+    import hashlib
+    import re
+    pat = re.compile(r"<!-- traffic kernel=(\S+) source=(\S+) sha256_16=([0-9a-f]{16}) dram_bytes_per_launch=(\d+) -->")
+    for name in sorted(os.listdir(PROFILES)) if os.path.isdir(PROFILES) else []:
+        with open(os.path.join(PROFILES, name)) as fh:
+            for m in pat.finditer(fh.read()):
+                if m.group(1) != kernel:
+                    continue
+                with open(os.path.join(CSRC, m.group(2)), "rb") as src:
+                    now = hashlib.sha256(src.read()).hexdigest()[:16]
+                if now != m.group(3):
+                    return None, f"stale: profiles/{name} profiled {m.group(2)} at {m.group(3)}, source is now {now}"
+                return int(m.group(4)), f"profiles/{name}"
+    return None, "no ncu capture of this kernel"
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -157,6 +183,12 @@ def decode_bytes(case) -> int:
     index key of every group is read once (L * G * Di * 2 per request)."""
     d = case.dims
     return int(sum(int(L) for L in case.seq_lens.tolist()) * d.G * d.Di * 2)
+
+
+def prefill_scoring_flops(case) -> float:
+    """Algorithmic flops of prefill index scoring: 2 * Di per (row, group, causally visible token)."""
+    d = case.dims
+    return float((case.q_pos.long() + 1).sum().item()) * d.G * 2 * d.Di
 
 
 def prefill_attention_flops(step, case) -> float:
@@ -189,6 +221,9 @@ def run_msa(args, rank, world, local):
         dec, case = bench_decode(args, rank, world, local, dev, peaks, peak_src)
         line.update(dec)
         line["decode_multi"] = bench_decode_multi(args, world, dev, peaks, peak_src)
+        if not args.no_sweep:
+            line["decode_sweep"] = {name: bench_decode_sweep(name, args, world, dev, peaks, peak_src)
+                                    for name in SWEEP}
     if args.only in ("all", "prefill"):
         line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src, rank)
     line["clocks"] = clocks.stop()
@@ -246,6 +281,7 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
     s1_ms = statistics.mean(s1_b[k].elapsed_time(s1_e[k]) for k in range(K))
     msa.msa_check(step.err)
     value = aggregate_throughput(B * K, world, dec_ms / 1e3)
+    tr, tr_src = ncu_traffic("k_score_decode")
     s1_bytes = decode_bytes(case)
     s1_gbs = s1_bytes / (s1_ms / 1e3) / 1e9
 
@@ -289,12 +325,71 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
                    "l2": "inputs larger than L2 (491.5 MB k-index scan per step)"},
         "gpu_launches": step.kernel_launches * K,
         "roofline": {"bound": "hbm", "kernel": "k_score_decode", "achieved": s1_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": s1_gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC["k_score_decode"],
+                     "unit": "GB/s", "frac": s1_gbs / peaks["hbm_gbs"], "traffic": tr, "traffic_source": tr_src,
                      "bytes_per_launch": s1_bytes, "ms_per_launch": s1_ms,
                      "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / K},
     }, case
+
+
+def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
+    """One decode workload besides the headline: decode1m (2 requests x 1,048,576 tokens) or a ragged
+    batch (1, 8, 32 or 64 requests of 4k-128k tokens).  Each timed step is one msa_decode_step with its
+    own CUDA-event pair; a 256 MB buffer is written between steps so that no step finds the previous
+    step's pages in L2 (a one-request batch reads less than L2 holds); the median step is reported.
+    Roofline: the step's algorithmic bytes -- every cached index key once plus the selected K and V
+    (row_len tokens of D bf16 each, per (request, group) row) -- over the median step time, against
+    the measured copy bandwidth."""
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+    K, W = args.steps, args.warmup
+    case = mi.named_case(name, device=dev)
+    dims = msa.dims_of(case)
+    B = case.n_rows
+    step = msa.DecodeStep(dims, B, case.n_req, case.n_pages, dev)
+    call = lambda: step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table,
+                        case.seq_lens, case.q_pos)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(W):
+        call()
+    msa.msa_check(step.err)
+    torch.cuda.synchronize()
+    barrier(world)
+    b_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for k in range(K):
+        flush.fill_(k & 0xff)
+        b_ev[k].record()
+        call()
+        e_ev[k].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    msa.msa_check(step.err)
+    ms = statistics.median(b_ev[k].elapsed_time(e_ev[k]) for k in range(K))
+    ms = max_over_ranks(ms, world, dev)
+    scan = decode_bytes(case)
+    kv = int(step.row_len.long().sum().item()) * dims.D * 2 * 2
+    gbs = (scan + kv) / (ms / 1e3) / 1e9
+    lens = case.seq_lens.tolist()
+    out = {
+        "metric": "MSA decode tok/s", "value": aggregate_throughput(B, world, ms / 1e3), "unit": "tok/s",
+        "ms_per_step": ms, "steps": K,
+        "config": {"workload": name, "batch": B, "ctx_min": int(min(lens)), "ctx_max": int(max(lens)),
+                   "ctx_total": int(sum(lens)), "Hq": dims.Hq, "G": dims.G, "D": dims.D, "Di": dims.Di,
+                   "topk": dims.topk, "l2": f"{L2_FLUSH_BYTES >> 20} MB written between timed steps",
+                   "timing": "median of per-step CUDA-event times"},
+        "gpu_launches": step.kernel_launches * K,
+        "roofline": {"bound": "hbm", "kernel": "msa_decode_step (index scan, select, attention)",
+                     "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": None, "traffic_source": "no ncu capture of this workload",
+                     "bytes_per_step": scan + kv, "index_bytes": scan, "kv_bytes": kv,
+                     "peak_source": f"{peak_src} hbm_gbs"},
+    }
+    del case, step, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
@@ -330,6 +425,7 @@ def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
         return max_over_ranks(a.elapsed_time(b), world, dev) / K
 
     multi_ms = timed(msa.MSA_PHASE_DECODE_MULTI)
+    tr, tr_src = ncu_traffic("k_score_decode_mt")
     row_ms = timed(msa.MSA_PHASE_DECODE)
     kbytes = sum(int(L) for L in case.seq_lens.tolist()) * dims.G * dims.Di * 2
     gbs = kbytes / (multi_ms / 1e3) / 1e9
@@ -339,7 +435,7 @@ def bench_decode_multi(args, world, dev, peaks, peak_src, T=8):
         "config": {"workload": f"decode60k with {T} query rows per request", "batch": 8, "rows": case.n_rows,
                    "ctx": 60000, "G": dims.G, "Di": dims.Di},
         "roofline": {"bound": "hbm", "kernel": "k_score_decode_mt", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": NCU_TRAFFIC["k_score_decode_mt"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": tr, "traffic_source": tr_src,
                      "bytes_per_launch": kbytes,
                      "peak_source": f"{peak_src} hbm_gbs"},
     }
@@ -364,24 +460,30 @@ def bench_prefill(args, world, dev, peaks, peak_src, rank=0):
         pcall()
     msa.msa_check(ps.err)
     torch.cuda.synchronize()
-    a_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    a_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    sel_ev, a_b, a_e, m_e = ev(), ev(), ev(), ev()
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     p0.record()
     for k in range(K):
+        sel_ev[k].record()
         ps.select(pc.q_idx, pc.kidx_cache, pc.block_table, pc.q_req, pc.q_pos)
         a_b[k].record()
         msa.msa_sparse_attn_prefill(pc.q, pc.k_cache, pc.v_cache, pc.block_table, pc.q_req, pc.q_pos,
                                     ps.blk_off, ps.blk_ent, pd, ps.o_part, ps.lse_part, ps.attn_ws, err_word=ps.err)
         a_e[k].record()
         msa.msa_lse_merge(ps.o_part, ps.lse_part, ps.sel, ps.ent_pos, pd, ps.out, ps.lse, err_word=ps.err)
+        m_e[k].record()
     p1.record()
     torch.cuda.synchronize()
     barrier(world)
     pre_ms = max_over_ranks(p0.elapsed_time(p1), world, dev)
     attn_ms = statistics.mean(a_b[k].elapsed_time(a_e[k]) for k in range(K))
+    sel_ms = statistics.mean(sel_ev[k].elapsed_time(a_b[k]) for k in range(K))
+    merge_ms = statistics.mean(a_e[k].elapsed_time(m_e[k]) for k in range(K))
+    sflops = prefill_scoring_flops(pc)
+    tr, tr_src = ncu_traffic("k_attn_prefill")
     msa.msa_check(ps.err)
     flops = prefill_attention_flops(ps, pc)
     tflops = flops / (attn_ms / 1e3) / 1e12
@@ -395,9 +497,16 @@ def bench_prefill(args, world, dev, peaks, peak_src, rank=0):
         "gpu_launches": ps.kernel_launches * K,
         "roofline": {"bound": "tensor", "kernel": "k_attn_prefill", "achieved": tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": tflops / peaks["bf16_tflops"], "traffic": NCU_TRAFFIC["k_attn_prefill"],
+                     "frac": tflops / peaks["bf16_tflops"], "traffic": tr, "traffic_source": tr_src,
                      "flops_per_launch": flops, "ms_per_launch": attn_ms,
                      "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "select": {"call": "msa_select_invert_prefill (tensor-core scoring with the top-k fused, list merge, "
+                           "inversion)" if ps.fuse_topk else "msa_index_score + msa_topk_blocks + msa_invert_selection",
+                   "ms_per_launch": sel_ms, "scoring_flops_per_launch": sflops,
+                   "scoring_tflops": sflops / (sel_ms / 1e3) / 1e12,
+                   "frac_of_bf16_peak": sflops / (sel_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "merge": {"kernel": "k_lse_merge", "ms_per_launch": merge_ms},
+        "timing": "CUDA events on the stream around each call, mean over the timed steps",
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         prefill["cpu_baseline"] = cpu_baseline_prefill(pc)
