@@ -226,6 +226,8 @@ def run_msa(args, rank, world, local):
                                     for name in SWEEP}
     if args.only in ("all", "prefill"):
         line["prefill"] = bench_prefill(args, world, dev, peaks, peak_src, rank)
+    if args.only == "all" and not args.no_sweep:
+        line["mixed"] = bench_mixed(args, world, dev)
     line["clocks"] = clocks.stop()
     if case is not None:
         line["cpu_baseline"] = (cpu_baseline_decode(rank, case=case)
@@ -388,6 +390,66 @@ def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
                      "peak_source": f"{peak_src} hbm_gbs"},
     }
     del case, step, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_mixed(args, world, dev):
+    """A chunked-prefill engine step: decode60k's batch (8 decode requests x 60,000 tokens) and
+    prefill68k's chunk (8,192 rows on a 60,000-token prefix) in ONE step over one page pool
+    (MixedStep).  Timed serially on one stream and with the decode half on a side stream; each
+    timed step has its own CUDA-event pair on the caller's stream (which joins the side stream
+    before the end event).  Reported: rows per second of the whole step (decode tokens plus
+    prefill rows), and both timings next to the two halves timed alone."""
+    import torch
+    import block_sparse_attention_06_gb300 as msa
+    import msa_inputs as mi
+    K, W = args.steps, args.warmup
+    dec, pre = mi.named_case("mixed", device=dev)
+    dims = msa.dims_of(dec)
+    margs = (dec.k_cache, dec.v_cache, dec.kidx_cache, dec.q, dec.q_idx, dec.block_table, dec.seq_lens, pre.q,
+             pre.q_idx, pre.block_table, pre.q_req, pre.q_pos)
+
+    def timed(fn, errs):
+        for _ in range(W):
+            fn()
+        for e in errs:
+            msa.msa_check(e)
+        torch.cuda.synchronize()
+        barrier(world)
+        b_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for k in range(K):
+            b_ev[k].record()
+            fn()
+            e_ev[k].record()
+        torch.cuda.synchronize()
+        barrier(world)
+        for e in errs:
+            msa.msa_check(e)
+        return max_over_ranks(statistics.median(b_ev[k].elapsed_time(e_ev[k]) for k in range(K)), world, dev)
+
+    res = {}
+    for overlap in (False, True):
+        ms = msa.MixedStep(dims, dec.n_rows, pre.n_rows, pre.n_req, dec.n_pages, dev, overlap=overlap)
+        res[overlap] = timed(lambda: ms(*margs), ms.err_words)
+    d_only = timed(lambda: ms.decode(dec.q, dec.q_idx, dec.k_cache, dec.v_cache, dec.kidx_cache, dec.block_table,
+                                     dec.seq_lens), [ms.decode.err])
+    p_only = timed(lambda: ms.prefill(pre.q, pre.q_idx, pre.k_cache, pre.v_cache, pre.kidx_cache, pre.block_table,
+                                      pre.q_req, pre.q_pos), [ms.prefill.err])
+    rows = dec.n_rows + pre.n_rows
+    best = min(res.values())
+    out = {
+        "metric": "MSA mixed step rows/s (decode tokens + prefill rows)",
+        "value": aggregate_throughput(rows, world, best / 1e3), "unit": "rows/s",
+        "ms_per_step": best, "ms_per_step_serial": res[False], "ms_per_step_overlapped": res[True],
+        "ms_decode_half_alone": d_only, "ms_prefill_half_alone": p_only,
+        "config": {"workload": "mixed: decode60k batch + prefill68k chunk over one pool", "decode_requests": dec.n_rows,
+                   "prefill_rows": pre.n_rows, "Hq": dims.Hq, "G": dims.G, "D": dims.D, "Di": dims.Di,
+                   "topk": dims.topk, "timing": "median of per-step CUDA-event times on the caller's stream"},
+        "gpu_launches": ms.kernel_launches * K,
+    }
+    del dec, pre, ms
     torch.cuda.empty_cache()
     return out
 

@@ -686,3 +686,46 @@ class PrefillStep:
     def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, q_req, q_pos):
         self.select(q_idx, kidx_cache, block_table, q_req, q_pos)
         return self.attend(q, k_cache, v_cache, block_table, q_req, q_pos)
+
+
+class MixedStep:
+    """One step of a chunked-prefill engine over ONE shared page pool: a batch of decode
+    requests (one new token each) and a prefill chunk of one or more requests.  Decode
+    rows take the decode path (index scan, top-k + page tables, paged attention:
+    msa_decode_step); chunk rows take the block-major path (tensor-core scoring with the
+    top-k fused, inversion, block-major attention, LSE merge: PrefillStep).  The two
+    halves share the K, V and k-index caches and read disjoint block-table rows.
+
+    With overlap=True the decode half runs on a side stream that forks from the caller's
+    current stream and joins it again before the call returns, so the HBM-bound decode
+    scan can run beside the prefill kernels where SM resources allow; otherwise both run
+    in order on the current stream.  Either way every result is produced by the same
+    kernels as the separate steps, so the outputs are bit-identical to them."""
+
+    def __init__(self, dims: Dims, n_decode: int, n_prefill_rows: int, n_prefill_req: int, n_pages: int, device,
+                 overlap: bool = True):
+        self.decode = DecodeStep(dims, n_decode, n_decode, n_pages, device)
+        self.prefill = PrefillStep(dims, n_prefill_rows, n_prefill_req, device)
+        self.overlap = bool(overlap)
+        self.device = torch.device(device)
+        self._side = torch.cuda.Stream(device=self.device) if self.overlap else None
+        self.kernel_launches = self.decode.kernel_launches + self.prefill.kernel_launches
+
+    @property
+    def err_words(self):
+        return (self.decode.err, self.prefill.err)
+
+    def __call__(self, k_cache, v_cache, kidx_cache, dec_q, dec_q_idx, dec_block_table, dec_seq_lens, pre_q,
+                 pre_q_idx, pre_block_table, pre_q_req, pre_q_pos):
+        """-> (decode out, decode lse, prefill out, prefill lse)"""
+        if not self.overlap:
+            self.decode(dec_q, dec_q_idx, k_cache, v_cache, kidx_cache, dec_block_table, dec_seq_lens)
+            self.prefill(pre_q, pre_q_idx, k_cache, v_cache, kidx_cache, pre_block_table, pre_q_req, pre_q_pos)
+            return self.decode.out, self.decode.lse, self.prefill.out, self.prefill.lse
+        main = torch.cuda.current_stream(self.device)
+        self._side.wait_stream(main)                 # inputs written on the caller's stream are visible
+        with torch.cuda.stream(self._side):
+            self.decode(dec_q, dec_q_idx, k_cache, v_cache, kidx_cache, dec_block_table, dec_seq_lens)
+        self.prefill(pre_q, pre_q_idx, k_cache, v_cache, kidx_cache, pre_block_table, pre_q_req, pre_q_pos)
+        main.wait_stream(self._side)                 # the decode results are complete on the caller's stream
+        return self.decode.out, self.decode.lse, self.prefill.out, self.prefill.lse

@@ -34,7 +34,7 @@ PAGE = 128
 
 __all__ = [
     "PAGE", "Dims", "Case", "decode_case", "prefill_case", "tiny_case",
-    "ragged_lengths", "named_case", "CONFIG_NAMES",
+    "ragged_lengths", "named_case", "CONFIG_NAMES", "mixed_case",
 ]
 
 
@@ -286,6 +286,70 @@ def ragged_prefill_case(prefixes: Sequence[int], chunks: Sequence[int], Hq: int,
                 torch.cat(parts_req), torch.cat(parts_pos), max_blocks, [], name)
 
 
+def mixed_case(decode_lens: Sequence[int], prefixes: Sequence[int], chunks: Sequence[int], Hq: int, G: int,
+               D: int, Di: int, topk: int, seed: int, device="cpu", pool_pages: Optional[int] = None,
+               needles_per_group: int = 4, span: int = 256, span_sigma: float = 0.5,
+               name: str = "") -> Tuple[Case, Case]:
+    """One step of a chunked-prefill engine: a batch that mixes decode requests (one new
+    token each) with a prefill chunk of one or more requests, over ONE shared page pool.
+
+    Requests 0 .. Bd-1 are the decode requests (request b holds decode_lens[b] tokens, its
+    query at position decode_lens[b] - 1, with needle blocks as in decode_case); requests
+    Bd .. Bd+Bp-1 are the prefill requests (request Bd + r appends chunks[r] rows at
+    positions prefixes[r] .. prefixes[r]+chunks[r]-1, with the span structure of
+    prefill_case for its query-side index vectors).  Returns (decode Case, prefill Case):
+    they share the cache tensors; the decode case's block table is rows 0 .. Bd-1 of the
+    joint table and the prefill case's rows Bd .., both views of one tensor, so q_req of a
+    prefill row counts from 0 within the prefill case."""
+    page = PAGE
+    dims = Dims(Hq, G, D, Di, topk, page)
+    Bd, Bp = len(decode_lens), len(chunks)
+    assert Bd > 0 and Bp > 0 and len(prefixes) == Bp
+    pre_lens = [p + c for p, c in zip(prefixes, chunks)]
+    lens = list(decode_lens) + pre_lens
+    if pool_pages is None:
+        pool_pages = int(math.ceil(1.1 * sum((L + page - 1) // page for L in lens))) + 8
+    gc = _gen(seed, "cpu")
+    bt, max_blocks = _place_pages(lens, pool_pages, page, gc)
+    gd = _gen(seed + 7919, device)
+    # decode rows
+    q_d = _randn_f32((Bd, Hq, D), gd, device).to(torch.bfloat16)
+    qi_d = _randn_f32((Bd, G, Di), gd, device).to(torch.bfloat16)
+    shifts: dict = {}
+    needles: List[Tuple[int, int, int]] = []
+    qi_cpu = qi_d.float().cpu()
+    for b, L in enumerate(decode_lens):
+        own = (L - 1) // page
+        for g in range(G):
+            u = _unit(qi_cpu[b, g])
+            for j in _pick_needles(own, needles_per_group, gc):
+                shifts.setdefault(int(bt[b, j]), []).append((g, 3.0 * u))
+                needles.append((b, g, j))
+    # prefill rows
+    n_rows = sum(chunks)
+    q_p = _randn_f32((n_rows, Hq, D), gd, device).to(torch.bfloat16)
+    parts_idx, parts_req, parts_pos = [], [], []
+    for r, (p0, c) in enumerate(zip(prefixes, chunks)):
+        n_span = (c + span - 1) // span
+        centres = _randn_f32((n_span, G, Di), gd, device)
+        noise = _randn_f32((c, G, Di), gd, device)
+        span_of_row = torch.arange(c, device=device) // span
+        parts_idx.append(centres[span_of_row] + span_sigma * noise)
+        parts_req.append(torch.full((c,), r, dtype=torch.int32, device=device))
+        parts_pos.append(torch.arange(p0, p0 + c, dtype=torch.int32, device=device))
+    kidx = _pool_bf16(pool_pages, page, G, Di, gd, device, shifts)
+    k_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    v_cache = _pool_bf16(pool_pages, page, G, D, gd, device)
+    btd = bt.to(device)
+    seq = torch.tensor(lens, dtype=torch.int32, device=device)
+    dec = Case(dims, k_cache, v_cache, kidx, btd[:Bd], seq[:Bd], q_d, qi_d,
+               torch.arange(Bd, dtype=torch.int32, device=device), (seq[:Bd] - 1).to(torch.int32), max_blocks,
+               needles, name + "-decode")
+    pre = Case(dims, k_cache, v_cache, kidx, btd[Bd:], seq[Bd:], q_p, torch.cat(parts_idx).to(torch.bfloat16),
+               torch.cat(parts_req), torch.cat(parts_pos), max_blocks, [], name + "-prefill")
+    return dec, pre
+
+
 def tiny_case(seed: int = 1000, device="cpu", L: int = 2048, n_decode: int = 16,
               Hq: int = 8, G: int = 2, D: int = 64, Di: int = 32, topk: int = 4,
               pool_pages: int = 32, needles_per_group: int = 2) -> Tuple[Case, Case]:
@@ -340,7 +404,7 @@ def ragged_lengths(B: int, seed: int, lo: int = 4096, hi: int = 131072) -> List[
 
 
 CONFIG_NAMES = ("tiny", "decode60k", "prefill68k", "ragged1", "ragged8", "ragged32",
-                "ragged64", "decode1m")
+                "ragged64", "decode1m", "mixed")
 
 
 def named_case(name: str, device="cpu"):
@@ -361,6 +425,9 @@ def named_case(name: str, device="cpu"):
         pool = int(math.ceil(1.25 * sum((L + PAGE - 1) // PAGE for L in lens)))
         return decode_case(lens, pool_pages=pool, needles_per_group=4, seed=1003,
                            device=device, name=name, **H)
+    if name == "mixed":
+        # decode60k's batch and prefill68k's chunk in one step over one pool
+        return mixed_case([60000] * 8, [60000], [8192], seed=1005, device=device, name=name, **H)
     if name == "decode1m":
         ranges = [(0.0, 0.05, 3), (0.475, 0.525, 3), (0.95, 1.0, 2)]
         return decode_case([1 << 20] * 2, pool_pages=16640, needles_per_group=8,
