@@ -261,9 +261,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
         bool ok = true;
         int it = 0;                                      // blocks over all passes
         const int own = p >> 7;                          // the row's own block (forced, not ranked)
-        uint64_t lst[kListLen];                          // fused top-k: best keys first, 0 = none
+        // fused top-k: the chunk's best candidates, best first, as (order-preserving score bits, block);
+        // a row meets its blocks in increasing block order, so on equal scores the entry already in the
+        // list ranks first and a strict compare of the score bits alone gives the (score desc, block asc)
+        // order of the 64-bit sort keys, which are built only when the list is written out
+        uint32_t lst_s[kListLen];                        // 0 = empty (every real score maps above 0)
+        int32_t lst_j[kListLen];
 #pragma unroll
-        for (int i = 0; i < kListLen; ++i) lst[i] = 0ull;
+        for (int i = 0; i < kListLen; ++i) {
+            lst_s[i] = 0u;
+            lst_j[i] = 0;
+        }
         for (int pk = 0; ok && pk < n_pass; ++pk) {
         const int req = sm.pass_req[pk], nblk = pass_end(pk) - j0;
         for (int jj = 0; jj < nblk; ++jj, ++it) {
@@ -276,20 +284,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             // leave the epilogue waiting on instruction latency)
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(lane_addr + uint32_t(acc * 128 + c0), v);
+            for (int c0 = 0; c0 < 128; c0 += 64) {   // two 32-column TMEM loads per wait
+                uint32_t v[2][32];
+                tmem_ld32(lane_addr + uint32_t(acc * 128 + c0), v[0]);
+                tmem_ld32(lane_addr + uint32_t(acc * 128 + c0 + 32), v[1]);
                 tmem_ld_wait();
-                if (lim < c0 + 31) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (c0 + i > lim) v[i] = __float_as_uint(-INFINITY);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int c1 = c0 + 32 * hh;
+                    if (lim < c1 + 31) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c1 + i > lim) v[hh][i] = __float_as_uint(-INFINITY);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mx[k] = fmax3(mx[k], __uint_as_float(v[hh][i + k]), __uint_as_float(v[hh][i + 4 + k]));
                 }
-#pragma unroll
-                for (int i = 0; i < 32; i += 8)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mx[k] = fmax3(mx[k], __uint_as_float(v[i + k]), __uint_as_float(v[i + 4 + k]));
             }
             const float best = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             tc_fence_before();
@@ -298,15 +311,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
             if (FUSED) {
                 const int jb = j0 + jj;
                 if (jb < own && (one_req || sm.row_req[row] == req)) {
-                    uint64_t key = topk_key(best, jb, err);
-                    if (key > lst[kListLen - 1]) {
-                        // sorted insertion: the key sinks to its place, the worst key drops out
+                    uint32_t ks = uint32_t(topk_key(best, jb, err) >> 32);
+                    if (ks > lst_s[kListLen - 1]) {
+                        // sorted insertion: the entry sinks to its place, the worst one drops out
+                        int kj = jb;
 #pragma unroll
                         for (int i = 0; i < kListLen; ++i) {
-                            const uint64_t cur = lst[i];
-                            const bool take = key > cur;
-                            lst[i] = take ? key : cur;
-                            key = take ? cur : key;
+                            const uint32_t cs = lst_s[i];
+                            const int32_t cj = lst_j[i];
+                            const bool take = ks > cs;
+                            lst_s[i] = take ? ks : cs;
+                            lst_j[i] = take ? kj : cj;
+                            ks = take ? cs : ks;
+                            kj = take ? cj : kj;
                         }
                     }
                 }
@@ -331,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
         if (FUSED && grow < n_rows) {
             uint64_t *o = list_of(row);
 #pragma unroll
-            for (int i = 0; i < kListLen; ++i) o[i] = lst[i];
+            for (int i = 0; i < kListLen; ++i)
+                o[i] = lst_s[i] ? (uint64_t(lst_s[i]) << 32) | uint64_t(~uint32_t(lst_j[i])) : 0ull;
         }
     }
 
