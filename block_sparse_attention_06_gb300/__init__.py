@@ -546,6 +546,37 @@ class DecodeStep:
                         self.sel, self.page_table, self.row_len, self.out, self.lse, self.workspace, self.err)
         return self.out, self.lse
 
+    def capture(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, inputs=None,
+                host_results=None):
+        """Record one whole step on these tensors into a CUDA graph and keep it for replay():
+        a serving engine replays the decode step instead of launching its kernels one by
+        one.  With `inputs` (a DecodeInputs whose device views are the tensors passed here)
+        the graph also holds that step's upload, and with `host_results` (from
+        host_results()) the download of out and lse.  The tensors are baked into the graph:
+        write new values into them, then replay().  One eager call runs first, so every
+        kernel's attributes are set before capture."""
+        args = (q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens)
+        if inputs is not None:
+            inputs.upload()
+        self(*args)
+        if host_results is not None:
+            self.download(host_results)
+        torch.cuda.synchronize(q.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            if inputs is not None:
+                inputs.upload()
+            self(*args)
+            if host_results is not None:
+                self.download(host_results)
+        self._graph = graph
+        return graph
+
+    def replay(self):
+        """Replay the step recorded by capture() on the current stream."""
+        self._graph.replay()
+        return self.out, self.lse
+
     def host_results(self):
         """Page-locked host buffer laid out like the device (out, lse) buffer, with
         its (out, lse) views; download() fills it."""

@@ -174,3 +174,36 @@ def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(msa):
     assert ei.value.status == 5 and "TIMEOUT" in str(ei.value)
     _, dec = mi.tiny_case(seed=1000, device=DEV)
     _check_decode(msa, dec)
+
+
+def test_decode_step_graph_replay(msa):
+    """DecodeStep.capture() records the whole step (and, with DecodeInputs and a host
+    result buffer, its upload and download) into a CUDA graph; replay() gives the same
+    bits as the eager step, and new inputs written into the captured tensors are picked
+    up by the next replay."""
+    case = mi.decode_case([700, 3000, 129, 60000], Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=600,
+                          needles_per_group=2, seed=19, device=DEV)
+    dims = msa.dims_of(case)
+    eager = msa.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    inputs = msa.DecodeInputs(dims, case.n_rows, DEV)
+    for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table"):
+        getattr(inputs, "h_" + n).copy_(getattr(case, n).cpu())
+    step = msa.DecodeStep(dims, case.n_rows, case.n_req, case.n_pages, DEV)
+    host_res, (h_out, h_lse) = step.host_results()
+    step.capture(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table,
+                 inputs.seq_lens, inputs=inputs, host_results=host_res)
+    gen = torch.Generator().manual_seed(3)
+    for it in range(3):
+        if it > 0:   # new queries for the next step, written into the pinned inputs the graph uploads
+            inputs.h_q.copy_(torch.randn(inputs.h_q.shape, generator=gen).to(torch.bfloat16))
+            inputs.h_q_idx.copy_(torch.randn(inputs.h_q_idx.shape, generator=gen).to(torch.bfloat16))
+        step.replay()
+        torch.cuda.synchronize()
+        msa.msa_check(step.err)
+        eager(inputs.h_q.to(DEV), inputs.h_q_idx.to(DEV), case.k_cache, case.v_cache, case.kidx_cache,
+              case.block_table, case.seq_lens)
+        msa.msa_check(eager.err)
+        torch.cuda.synchronize()
+        for name in ("sel", "page_table", "row_len", "out", "lse"):
+            assert torch.equal(getattr(step, name), getattr(eager, name)), (it, name)
+        assert torch.equal(h_out, eager.out.cpu()) and torch.equal(h_lse, eager.lse.cpu()), it
