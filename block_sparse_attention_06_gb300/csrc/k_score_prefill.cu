@@ -313,18 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_score_prefill(
                 if (jb < own && (one_req || sm.row_req[row] == req)) {
                     uint32_t ks = uint32_t(topk_key(best, jb, err) >> 32);
                     if (ks > lst_s[kListLen - 1]) {
-                        // sorted insertion: the entry sinks to its place, the worst one drops out
-                        int kj = jb;
+                        // sorted insertion without a dependency chain: the entries below the new one
+                        // (gt[i], a suffix of the list) move down one slot and the first of them takes
+                        // the new entry; the worst one drops out
+                        bool gt[kListLen];
 #pragma unroll
-                        for (int i = 0; i < kListLen; ++i) {
-                            const uint32_t cs = lst_s[i];
-                            const int32_t cj = lst_j[i];
-                            const bool take = ks > cs;
-                            lst_s[i] = take ? ks : cs;
-                            lst_j[i] = take ? kj : cj;
-                            ks = take ? cs : ks;
-                            kj = take ? cj : kj;
+                        for (int i = 0; i < kListLen; ++i) gt[i] = ks > lst_s[i];
+#pragma unroll
+                        for (int i = kListLen - 1; i >= 1; --i) {
+                            lst_s[i] = gt[i] ? (gt[i - 1] ? lst_s[i - 1] : ks) : lst_s[i];
+                            lst_j[i] = gt[i] ? (gt[i - 1] ? lst_j[i - 1] : jb) : lst_j[i];
                         }
+                        lst_s[0] = gt[0] ? ks : lst_s[0];
+                        lst_j[0] = gt[0] ? jb : lst_j[0];
                     }
                 }
                 continue;
