@@ -34,7 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "block_sparse_attention_06_gb300", "csrc")
 SWEEP = ("decode1m", "ragged1", "ragged8", "ragged32", "ragged64")
-L2_FLUSH_BYTES = 256 << 20   # written between timed steps of the small workloads (L2 is 129 MB)
+L2_FLUSH_BYTES = 256 << 20   # read between timed steps of the small workloads (L2 is 129 MB)
 
 
 def parse_args():
@@ -347,9 +347,10 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
 
 def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
     """One decode workload besides the headline: decode1m (2 requests x 1,048,576 tokens) or a ragged
-    batch (1, 8, 32 or 64 requests of 4k-128k tokens).  Each timed step is one msa_decode_step with its
-    own CUDA-event pair; a 256 MB buffer is written between steps so that no step finds the previous
-    step's pages in L2 (a one-request batch reads less than L2 holds); the median step is reported.
+    batch (1, 8, 32 or 64 requests of 4k-128k tokens).  Each timed step is one msa_decode_step replayed
+    from a CUDA graph, with its own CUDA-event pair; a 256 MB buffer is read between steps so that no
+    step finds the previous step's pages in L2 (a one-request batch reads less than L2 holds) -- read,
+    not written, so that no dirty lines are written back during the next step; the median is reported.
     Roofline: the step's algorithmic bytes -- every cached index key once plus the selected K and V
     (row_len tokens of D bf16 each, per (request, group) row) -- over the median step time, against
     the measured copy bandwidth."""
@@ -361,9 +362,10 @@ def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
     dims = msa.dims_of(case)
     B = case.n_rows
     step = msa.DecodeStep(dims, B, case.n_req, case.n_pages, dev)
-    call = lambda: step(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table,
-                        case.seq_lens, case.q_pos)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step.capture(case.q, case.q_idx, case.k_cache, case.v_cache, case.kidx_cache, case.block_table,
+                 case.seq_lens)
+    call = step.replay
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(W):
         call()
     msa.msa_check(step.err)
@@ -372,7 +374,7 @@ def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
     b_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for k in range(K):
-        flush.fill_(k & 0xff)
+        flush.sum(dtype=torch.int32)   # evicts the previous step's lines from L2
         b_ev[k].record()
         call()
         e_ev[k].record()
@@ -390,8 +392,8 @@ def bench_decode_sweep(name, args, world, dev, peaks, peak_src):
         "ms_per_step": ms, "steps": K,
         "config": {"workload": name, "batch": B, "ctx_min": int(min(lens)), "ctx_max": int(max(lens)),
                    "ctx_total": int(sum(lens)), "Hq": dims.Hq, "G": dims.G, "D": dims.D, "Di": dims.Di,
-                   "topk": dims.topk, "l2": f"{L2_FLUSH_BYTES >> 20} MB written between timed steps",
-                   "timing": "median of per-step CUDA-event times"},
+                   "topk": dims.topk, "l2": f"{L2_FLUSH_BYTES >> 20} MB read between timed steps",
+                   "timing": "median of per-step CUDA-event times, the step replayed from a CUDA graph"},
         "gpu_launches": step.kernel_launches * K,
         "roofline": {"bound": "hbm", "kernel": "msa_decode_step (index scan, select, attention)",
                      "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
