@@ -181,6 +181,110 @@ __global__ void __launch_bounds__(256) k_topk_merge(const uint64_t *__restrict__
     }
 }
 
+// The same merge with one thread per (row, group), for rows of at most NC chunks.  Each chunk's
+// list is sorted best first, so the best k - 1 of the row are the first k - 1 keys of a k-way
+// merge of the lists: every step takes the largest of the NC list heads and moves that list on.
+// A thread keeps the next kMergeWin keys of every list in registers and reloads one key per step,
+// which arrives while the list's other kMergeWin - 1 keys are taken, so a step seldom waits on
+// memory.  The chosen ids are then put in ascending order by a sorting network; a missing
+// candidate (key 0) gives id -1, which sorts first, as in k_topk_merge.
+constexpr int kMergeWin = 4;
+
+__device__ __forceinline__ void cmp_swap(int &a, int &b) {
+    const int lo = min(a, b), hi = max(a, b);
+    a = lo;
+    b = hi;
+}
+
+template <int NC>
+__global__ void __launch_bounds__(256) k_topk_merge_heads(const uint64_t *__restrict__ lists,
+                                                          const int32_t *__restrict__ q_pos, int n_rows, int G,
+                                                          int max_blocks, int topk, int32_t *__restrict__ sel,
+                                                          InvMark mark, int32_t *err) {
+    constexpr int L = kSelectListLen;
+    constexpr int W = kMergeWin;
+    static_assert(L + 1 == 16, "the sorting network orders 16 ids");
+    static_assert(W <= L, "the window lies inside a list");
+    const int item = blockIdx.x * blockDim.x + threadIdx.x;
+    if (item >= n_rows * G) return;
+    const int r = item / G;
+    int32_t *out = sel + size_t(item) * topk;
+    const int p = q_pos[r];
+    if (p < 0 || (p >> 7) >= max_blocks) {
+        for (int i = 0; i < topk; ++i) out[i] = -1;
+        raise_flag(err, MSA_FLAG_BOUNDS);
+        return;
+    }
+    const int own = p >> 7;
+    const int k_eff = min(topk, own + 1);
+    const int n = k_eff - 1;                        // non-own blocks to choose, <= L
+    const uint64_t *l = lists + size_t(item) * NC * L;
+    uint64_t win[NC][W];                            // win[c][0] is the head of list c
+    int nxt[NC];                                    // list index of the key after the window
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) win[c][k] = l[c * L + k];
+        nxt[c] = W;
+    }
+    int id[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) id[t] = INT_MAX;   // past n: sorts last, never written
+#pragma unroll
+    for (int t = 0; t < L; ++t) {
+        if (t >= n) break;
+        uint64_t best = win[0][0];
+        int cb = 0;
+#pragma unroll
+        for (int c = 1; c < NC; ++c)
+            if (win[c][0] > best) {
+                best = win[c][0];
+                cb = c;
+            }
+        id[t] = best ? int(~uint32_t(best)) : -1;
+        if (best) {
+            // one load for the list the key came from, then its window moves on by one
+            int at = nxt[0];
+#pragma unroll
+            for (int c = 1; c < NC; ++c) at = c == cb ? nxt[c] : at;
+            const uint64_t fresh = at < L ? l[cb * L + at] : 0ull;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const bool take = c == cb;
+#pragma unroll
+                for (int k = 0; k < W - 1; ++k) win[c][k] = take ? win[c][k + 1] : win[c][k];
+                win[c][W - 1] = take ? fresh : win[c][W - 1];
+                nxt[c] += take ? 1 : 0;
+            }
+        }
+    }
+    // Batcher's odd-even merge sort of 16 ids, ascending
+#pragma unroll
+    for (int k = 2; k <= 16; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int m = i ^ j;
+                if (m > i) {
+                    if ((i & k) == 0) cmp_swap(id[i], id[m]);
+                    else cmp_swap(id[m], id[i]);
+                }
+            }
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+        if (t < n) out[t] = id[t];
+    out[n] = own;
+    for (int i = k_eff; i < topk; ++i) out[i] = -1;
+    if (mark.bitmap) {
+        const int g = item - r * G;
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            if (t < n) inv_mark_one(mark.bitmap, mark.words, mark.q_req, mark.n_req, max_blocks, r, g, id[t], err);
+        inv_mark_one(mark.bitmap, mark.words, mark.q_req, mark.n_req, max_blocks, r, g, own, err);
+    }
+}
+
 // One CTA of NT threads per (row, group) for long contexts: each warp keeps its
 // own best k-1, then warp 0 picks the best k-1 of those.
 template <int NT, int PER>
@@ -510,6 +614,18 @@ cudaError_t launch_topk_merge(const uint64_t *lists, const int32_t *q_pos, int n
     if (n_rows <= 0) return cudaSuccess;
     const int n_cand = n_chunks * kSelectListLen;
     const long long warps = 1LL * n_rows * s.G;
+    if (n_chunks <= 8) {
+        const unsigned tblocks = unsigned((warps + 255) / 256);
+#define MSA_TMH_CASE(NC)                                                                                   \
+    if (n_chunks == NC) {                                                                                  \
+        k_topk_merge_heads<NC><<<tblocks, 256, 0, st>>>(lists, q_pos, n_rows, s.G, s.max_blocks, s.topk, sel, \
+                                                        mark, err);                                        \
+        return cudaGetLastError();                                                                         \
+    }
+        MSA_TMH_CASE(1) MSA_TMH_CASE(2) MSA_TMH_CASE(3) MSA_TMH_CASE(4)
+        MSA_TMH_CASE(5) MSA_TMH_CASE(6) MSA_TMH_CASE(7) MSA_TMH_CASE(8)
+#undef MSA_TMH_CASE
+    }
     const unsigned blocks = unsigned((warps + 7) / 8);
 #define MSA_TM_CASE(PP)                                                                                     \
     if (n_cand <= 32 * PP) {                                                                                \
