@@ -369,47 +369,7 @@ __device__ __forceinline__ void emit_decode_row(uint64_t best, int item, int b, 
     if (lane == 0) row_len[item] = tok;
 }
 
-// One warp per (request, group) row, candidates in registers (PER per lane).
-template <int PER>
-__global__ void __launch_bounds__(256) k_decode_select_warp(
-    const float *__restrict__ scores, const int32_t *__restrict__ seq_lens,
-    const int32_t *__restrict__ block_table, int B, int G, int max_blocks, int topk, int n_pages,
-    int32_t *__restrict__ sel, int32_t *__restrict__ pt, int32_t *__restrict__ row_len,
-    int32_t *__restrict__ counters, int32_t *err) {
-    pdl_wait();   // the scores come from the scan kernel
-    pdl_trigger();
-    const int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (item >= B * G) return;
-    if (counters && lane == 0) counters[item] = 0;
-    const int b = item / G;
-    const int L = seq_lens[b];
-    const int p = L - 1;
-    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= 32 * PER) {
-        for (int i = lane; i < topk; i += 32) {
-            sel[size_t(item) * topk + i] = -1;
-            pt[size_t(item) * topk + i] = -1;
-        }
-        if (lane == 0) {
-            row_len[item] = 0;
-            raise_flag(err, MSA_FLAG_BOUNDS);
-        }
-        return;
-    }
-    const int own = p >> 7;
-    const int k_eff = min(topk, own + 1);
-    const float *s = scores + size_t(item) * max_blocks;
-    uint64_t keys[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int j = lane + 32 * i;
-        keys[i] = j < own ? topk_key(s[j], j, err) : 0ull;
-    }
-    const uint64_t best = warp_top_n<PER>(keys, k_eff - 1);
-    emit_decode_row(best, item, b, L, own, k_eff, topk, max_blocks, n_pages, block_table, sel, pt, row_len, err);
-}
-
-// One CTA of NT threads per row for long contexts.
+// One CTA of NT threads per (request, group) row, PER candidates per thread.
 template <int NT, int PER>
 __global__ void __launch_bounds__(NT) k_decode_select_cta(
     const float *__restrict__ scores, const int32_t *__restrict__ seq_lens,
@@ -685,17 +645,17 @@ cudaError_t launch_decode_select(const float *scores, const int32_t *seq_lens, c
     const int items = B * s.G;
     if (items <= 0) return cudaSuccess;
     const int mb = s.max_blocks;
-    const dim3 wgrid(unsigned((items + 7) / 8)), wblock(256);
 #define MSA_DSEL_ARGS scores, seq_lens, block_table, B, s.G, mb, s.topk, n_pages, sel, pt, row_len, counters, err
-    if (mb <= 128) return launch_kernel(k_decode_select_warp<4>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
-    if (mb <= 512) return launch_kernel(k_decode_select_warp<16>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
-    if (mb <= 1024) return launch_kernel(k_decode_select_warp<32>, wgrid, wblock, 0, st, pdl, MSA_DSEL_ARGS);
-    if (mb <= 8192)
-        return launch_kernel(k_decode_select_cta<256, 32>, dim3(unsigned(items)), dim3(256), 0, st, pdl,
+    // a CTA per row, one candidate per thread up to 512 blocks: a round of the per-warp top-k is then
+    // two warp reductions, where a warp holding 16 candidates per lane rescans them every round; at
+    // most 512 threads, so that warp 0's merge of the warps' lists (16 keys a lane) needs no spill
+#define MSA_DSEL_CTA(NT, PER)                                                                             \
+    if (mb <= (NT) * (PER))                                                                               \
+        return launch_kernel(k_decode_select_cta<NT, PER>, dim3(unsigned(items)), dim3(NT), 0, st, pdl,   \
                              MSA_DSEL_ARGS);
-    if (mb <= 16384)
-        return launch_kernel(k_decode_select_cta<512, 32>, dim3(unsigned(items)), dim3(512), 0, st, pdl,
-                             MSA_DSEL_ARGS);
+    MSA_DSEL_CTA(128, 1) MSA_DSEL_CTA(256, 1) MSA_DSEL_CTA(512, 1) MSA_DSEL_CTA(512, 2)
+    MSA_DSEL_CTA(512, 4) MSA_DSEL_CTA(512, 8) MSA_DSEL_CTA(512, 16) MSA_DSEL_CTA(512, 32)
+#undef MSA_DSEL_CTA
 #undef MSA_DSEL_ARGS
     return cudaErrorNotSupported;
 }
