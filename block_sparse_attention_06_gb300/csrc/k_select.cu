@@ -64,21 +64,54 @@ __device__ __forceinline__ int rank_ascending(int id, int n) {
     return rank;
 }
 
-// CTA-wide top-n: every warp reduces its own keys to its n best, then warp 0
-// takes the n best of those.  Returns, in warp 0, the lane's key as warp_top_n
-// does; other warps return 0.  `stage` holds NT keys of shared memory.
+// Bitonic sort of one key per lane, descending: lane i ends with the i-th largest of
+// the warp's 32 keys (five merge levels, fifteen exchange steps).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t k) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, k, stride);
+            // blocks of `size` alternate direction; the last level (size 32) runs descending
+            const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
+            k = keep_max ? max_u64(k, o) : (k < o ? k : o);
+        }
+    return k;
+}
+
+// CTA-wide top-n: every warp reduces its own keys to its n best, sorted best
+// first, then warp 0 merges those NW sorted lists: lane w holds the head of warp
+// w's list, each round takes the warp maximum of the heads and only the lane it
+// came from moves on.  Returns, in warp 0, the lane's key as warp_top_n does;
+// other warps return 0.  `stage` holds NT keys of shared memory.
 template <int NT, int PER>
 __device__ __forceinline__ uint64_t cta_top_n(const uint64_t (&keys)[PER], int n, uint64_t *stage) {
     constexpr int NW = NT / 32;
-    const int tid = threadIdx.x;
-    stage[tid] = warp_top_n<PER>(keys, n);
+    static_assert(NW <= 32, "one list per lane of warp 0");
+    const int tid = threadIdx.x, lane = tid & 31;
+    if constexpr (PER == 1) {
+        const uint64_t k = warp_sort_desc(keys[0]);
+        stage[tid] = lane < n ? k : 0ull;
+    } else {
+        stage[tid] = warp_top_n<PER>(keys, n);
+    }
     __syncthreads();
     uint64_t mine = 0;
     if (tid < 32) {
-        uint64_t k2[NW];
-#pragma unroll
-        for (int w = 0; w < NW; ++w) k2[w] = stage[tid + 32 * w];
-        mine = warp_top_n<NW>(k2, n);
+        int pos = 0;
+        uint64_t head = lane < NW ? stage[lane * 32] : 0ull;
+        for (int round = 0; round < n; ++round) {
+            const uint32_t hi = uint32_t(head >> 32);
+            const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+            const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? uint32_t(head) : 0u);
+            const uint64_t best = (uint64_t(mhi) << 32) | mlo;
+            if (lane == round) mine = best;
+            if (best != 0ull && head == best) {
+                ++pos;
+                head = pos < n ? stage[lane * 32 + pos] : 0ull;
+            }
+        }
     }
     return mine;
 }
@@ -377,15 +410,25 @@ __global__ void __launch_bounds__(NT) k_decode_select_cta(
     int32_t *__restrict__ sel, int32_t *__restrict__ pt, int32_t *__restrict__ row_len,
     int32_t *__restrict__ counters, int32_t *err) {
     __shared__ uint64_t stage[NT];
-    pdl_wait();
-    pdl_trigger();
     const int item = blockIdx.x;
     const int tid = threadIdx.x;
-    if (counters && tid == 0) counters[item] = 0;
     const int b = item / G;
+    // seq_lens and the block table are inputs of the step, not results of the scan: read them
+    // (the block table's row into L2) while the scan still runs
     const int L = seq_lens[b];
     const int p = L - 1;
-    if (p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= NT * PER) {
+    const bool bad = p < 0 || (p >> 7) >= max_blocks || (p >> 7) >= NT * PER;
+    if (!bad) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int j = tid + NT * i;
+            if (j <= (p >> 7) && (j & 31) == 0) prefetch_l2(block_table + size_t(b) * max_blocks + j);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (counters && tid == 0) counters[item] = 0;
+    if (bad) {
         for (int i = tid; i < topk; i += NT) {
             sel[size_t(item) * topk + i] = -1;
             pt[size_t(item) * topk + i] = -1;

@@ -67,6 +67,11 @@ __device__ __forceinline__ uint64_t topk_key(float s, int j, int32_t *err) {
     return (uint64_t(ord) << 32) | uint64_t(~uint32_t(j));
 }
 
+// Fetch the 128-byte line holding p into L2 (no register result, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------------ shared memory / mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
