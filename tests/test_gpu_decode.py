@@ -121,6 +121,18 @@ def test_decode1m(msa):
     assert hit >= int(0.9 * len(case.needles))
 
 
+@pytest.mark.parametrize("blocks", [150, 901, 1800, 3001, 10000])
+def test_decode_selection_tiers(msa, blocks):
+    """The decode selection kernel's launch shapes by context length: a CTA per (request,
+    group) row of 256 threads (up to 256 blocks), then 512 threads holding 2, 4, 8 or 32
+    candidates each; a short request shares every batch."""
+    lens = [blocks * 128 - 37, 3000]
+    case = mi.decode_case(lens, Hq=8, G=2, D=64, Di=32, topk=16, pool_pages=blocks + 40, needles_per_group=3,
+                          seed=600 + blocks, device=DEV)
+    assert case.max_blocks == blocks
+    _check_decode(msa, case)
+
+
 def test_out_of_range_page_is_flagged(msa):
     case = mi.decode_case([600, 900], Hq=16, G=2, D=128, Di=64, topk=4, pool_pages=20, needles_per_group=1,
                           seed=3, device=DEV)

@@ -175,6 +175,13 @@ def _fused_cases():
     yield "g8_k16", lambda: mi.prefill_case(2100, 400, Hq=32, G=8, D=128, Di=64, topk=16, pool_pages=40, seed=13,
                                             device=DEV)
     yield "prefill68k", lambda: mi.named_case("prefill68k", device=DEV)
+    # rows of 7 and 8 chunk lists (the per-thread k-way merge at its widest) and of 9 (the warp merge)
+    yield "chunks7", lambda: mi.prefill_case(110000, 300, Hq=16, G=2, D=64, Di=32, topk=16, pool_pages=900, seed=31,
+                                             device=DEV)
+    yield "chunks8", lambda: mi.prefill_case(126000, 300, Hq=16, G=2, D=64, Di=32, topk=16, pool_pages=1000,
+                                             seed=32, device=DEV)
+    yield "chunks9", lambda: mi.prefill_case(140000, 300, Hq=16, G=2, D=64, Di=32, topk=16, pool_pages=1100,
+                                             seed=33, device=DEV)
 
 
 @pytest.mark.parametrize("name,make", list(_fused_cases()), ids=[n for n, _ in _fused_cases()])
