@@ -294,8 +294,9 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
     s1_gbs = s1_bytes / (s1_ms / 1e3) / 1e9
 
     # ---------------- e2e through the public API: pinned host inputs in, result out.
-    # The step's inputs sit packed in one page-locked buffer (msa.DecodeInputs) and go
-    # up in one copy; out and lse come back in one copy.
+    # The step's inputs sit packed in one page-locked buffer (msa.DecodeInputs) and go up
+    # by one staging kernel (msa_stage_from_host); the attention kernel writes out and lse
+    # straight into a page-locked host buffer.
     inputs = msa.DecodeInputs(dims, B, dev)
     for n in ("q", "q_idx", "q_pos", "seq_lens", "block_table"):
         getattr(inputs, "h_" + n).copy_(getattr(case, n).cpu())
@@ -307,7 +308,7 @@ def bench_decode(args, rank, world, local, dev, peaks, peak_src):
     e2e_graph.capture(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table,
                       inputs.seq_lens, inputs=inputs, host_results=host_res)
 
-    def e2e_step():   # one replay = upload of the step's inputs, the step, download of out and lse
+    def e2e_step():   # one replay = upload of the step's inputs, the step, out and lse into host memory
         e2e_graph.replay()
 
     for _ in range(W):

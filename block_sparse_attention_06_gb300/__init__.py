@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "msa_sparse_attn_decode": [P, P, P, P, P, I, I, D, P, P, P, S, P, P],
         "msa_decode_step": [P, P, P, P, P, P, P, I, I, D, P, P, P, P, P, P, P, S, P, P],
         "msa_offload_gather": [P, P, I, P, I, D, P, P, P, P, P],
+        "msa_stage_from_host": [P, P, S, P],
         "msa_select_prefill": [P, P, P, P, P, I, I, I, D, P, P, S, P, P],
         "msa_check": [P, P],
     }
@@ -115,6 +116,18 @@ def _call(name: str, *args):
     rc = getattr(_lib, name)(*args)
     if rc != 0:
         raise MsaError(rc, name, _lib.msa_last_error().decode(errors="replace"))
+
+
+def _req_result(t: torch.Tensor, dtype, name: str, shape=None):
+    """A decode result buffer: a CUDA tensor, or a page-locked CPU tensor that the attention
+    kernel writes directly over the host link."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or page-locked (pinned) host memory")
+        if t.dtype != dtype or not t.is_contiguous() or (shape is not None and tuple(t.shape) != tuple(shape)):
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
+        return t
+    return _req(t, dtype, name, shape)
 
 
 def _req(t: torch.Tensor, dtype, name: str, shape=None):
@@ -389,8 +402,8 @@ def msa_sparse_attn_decode(q, k_cache, v_cache, page_table, row_len, dims: Dims,
         out = torch.empty((B, dims.Hq, dims.D), dtype=torch.bfloat16, device=dev)
     if lse is None:
         lse = torch.empty((B, dims.Hq), dtype=torch.float32, device=dev)
-    _req(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
-    _req(lse, torch.float32, "lse", (B, dims.Hq))
+    _req_result(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
+    _req_result(lse, torch.float32, "lse", (B, dims.Hq))
     need = msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
@@ -464,8 +477,8 @@ def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_len
     _req(sel, torch.int32, "sel", (B, dims.G, dims.topk))
     _req(page_table, torch.int32, "page_table", (B * dims.G, dims.topk))
     _req(row_len, torch.int32, "row_len", (B * dims.G,))
-    _req(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
-    _req(lse, torch.float32, "lse", (B, dims.Hq))
+    _req_result(out, torch.bfloat16, "out", (B, dims.Hq, dims.D))
+    _req_result(lse, torch.float32, "lse", (B, dims.Hq))
     need = msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, **f)
@@ -541,46 +554,57 @@ class DecodeStep:
         return msa_sparse_attn_decode(q, pk, pv, ppt, self.row_len, self.dims, self.out, self.lse, self.workspace,
                                       err_word=self.err)
 
-    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos=None):
+    def __call__(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, q_pos=None, out=None,
+                 lse=None):
+        """The step through msa_decode_step; out and lse default to the step's device buffers
+        and may be page-locked host views (host_results()), which the step then writes directly."""
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
         msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, self.dims, self.scores,
-                        self.sel, self.page_table, self.row_len, self.out, self.lse, self.workspace, self.err)
-        return self.out, self.lse
+                        self.sel, self.page_table, self.row_len, out, lse, self.workspace, self.err)
+        return out, lse
 
     def capture(self, q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens, inputs=None,
                 host_results=None):
         """Record one whole step on these tensors into a CUDA graph and keep it for replay():
         a serving engine replays the decode step instead of launching its kernels one by
         one.  With `inputs` (a DecodeInputs whose device views are the tensors passed here)
-        the graph also holds that step's upload, and with `host_results` (from
-        host_results()) the download of out and lse.  The tensors are baked into the graph:
-        write new values into them, then replay().  One eager call runs first, so every
-        kernel's attributes are set before capture."""
+        the graph also holds that step's upload, and with `host_results` (the buffer from
+        host_results()) the attention kernel writes out and lse straight into that
+        page-locked buffer, so they need no copy of their own.  The tensors are baked into
+        the graph: write new values into them, then replay().  One eager call runs first,
+        so every kernel's attributes are set before capture."""
         args = (q, q_idx, k_cache, v_cache, kidx_cache, block_table, seq_lens)
+        res = {}
+        if host_results is not None:
+            _, (h_out, h_lse) = self._host_views(host_results)
+            res = dict(out=h_out, lse=h_lse)
         if inputs is not None:
             inputs.upload()
-        self(*args)
-        if host_results is not None:
-            self.download(host_results)
+        self._graph_results = self(*args, **res)
         torch.cuda.synchronize(q.device)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             if inputs is not None:
                 inputs.upload()
-            self(*args)
-            if host_results is not None:
-                self.download(host_results)
+            self(*args, **res)
         self._graph = graph
         return graph
 
     def replay(self):
-        """Replay the step recorded by capture() on the current stream."""
+        """Replay the step recorded by capture() on the current stream; returns the (out,
+        lse) it writes (the host views when it was captured with host_results)."""
         self._graph.replay()
-        return self.out, self.lse
+        return self._graph_results
 
     def host_results(self):
-        """Page-locked host buffer laid out like the device (out, lse) buffer, with
-        its (out, lse) views; download() fills it."""
+        """Page-locked host buffer laid out like the device (out, lse) buffer, with its
+        (out, lse) views: download() fills it from the device buffer, and a step given the
+        views (or captured with the buffer) writes them directly."""
         buf = torch.empty(self._out_buf.shape, dtype=torch.uint8).pin_memory()
+        return self._host_views(buf)
+
+    def _host_views(self, buf):
         return buf, _views(buf, [(tuple(self.out.shape), self.out.dtype), (tuple(self.lse.shape), self.lse.dtype)])
 
     def download(self, host_buf):
@@ -613,12 +637,28 @@ def _packed(specs, device):
     return buf, _views(buf, specs)
 
 
+def msa_stage_from_host(host: torch.Tensor, dev: torch.Tensor) -> torch.Tensor:
+    """Copy the bytes of a page-locked host tensor into a device tensor of the same byte
+    size with the staging kernel of msa_stage_from_host (16-byte loads reading the host
+    buffer in place), queued on the current stream."""
+    if host.is_cuda or not host.is_pinned():
+        raise ValueError("host must be a page-locked CPU tensor")
+    if not host.is_contiguous():
+        raise ValueError("host must be contiguous")
+    _req(dev, dev.dtype, "dev")
+    n = host.numel() * host.element_size()
+    if dev.numel() * dev.element_size() != n:
+        raise ValueError(f"dev holds {dev.numel() * dev.element_size()} bytes, host {n}")
+    _call("msa_stage_from_host", _ptr(host), _ptr(dev), n, _stream(dev.device))
+    return dev
+
+
 class DecodeInputs:
     """The per-step inputs of a decode step for B requests -- q, q_idx, seq_lens,
     q_pos and block_table -- packed in one page-locked host buffer and one device
-    buffer of the same layout, so a step's host-to-device traffic is a single copy
-    (upload) instead of one copy per tensor.  Fill the host views (h_q, ...), call
-    upload(), then pass the device views (q, ...) to DecodeStep."""
+    buffer of the same layout, so a step's host-to-device traffic is one staging kernel
+    (upload, msa_stage_from_host) instead of one copy per tensor.  Fill the host views
+    (h_q, ...), call upload(), then pass the device views (q, ...) to DecodeStep."""
 
     def __init__(self, dims: Dims, B: int, device):
         specs = [((B, dims.Hq, dims.D), torch.bfloat16), ((B, dims.G, dims.Di), torch.bfloat16),
@@ -633,8 +673,10 @@ class DecodeInputs:
         return self.host.numel()
 
     def upload(self):
-        """Queue one host-to-device copy of all inputs on the current stream."""
-        self.dev.copy_(self.host, non_blocking=True)
+        """Queue the host-to-device copy of all inputs on the current stream: one staging
+        kernel reads the page-locked buffer over the host link (a copy-engine transfer of
+        these few hundred KB costs about 10 us more per step on a Grace-Blackwell node)."""
+        msa_stage_from_host(self.host, self.dev)
 
 
 class PrefillStep:

@@ -63,7 +63,40 @@ __global__ void __launch_bounds__(kThreads) k_offload_gather(const uint4 *__rest
     }
 }
 
+// A step's inputs staged from page-locked host memory by SM loads over the host link.
+// A copy-engine transfer of a decode step's inputs (about 155 KB for 8 requests)
+// carries a fixed cost of about 10 us on this link; a grid of 16-byte loads, each
+// thread's loads issued before its stores, moves them in roughly one round trip.
+constexpr int kStagePer = 4;   // 16-byte pieces per thread
+
+__global__ void __launch_bounds__(kThreads) k_stage_from_host(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                              size_t n) {
+    const size_t base = size_t(blockIdx.x) * kThreads * kStagePer + threadIdx.x;
+    uint4 v[kStagePer];
+#pragma unroll
+    for (int i = 0; i < kStagePer; ++i) {
+        const size_t x = base + size_t(i) * kThreads;
+        if (x < n) v[i] = src[x];
+    }
+#pragma unroll
+    for (int i = 0; i < kStagePer; ++i) {
+        const size_t x = base + size_t(i) * kThreads;
+        if (x < n) dst[x] = v[i];
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stage_from_host(const void *src, void *dst, size_t bytes, cudaStream_t st) {
+    const size_t n = bytes / 16;
+    if (n == 0) return cudaSuccess;
+    const size_t per_cta = size_t(kThreads) * kStagePer;
+    const size_t grid = (n + per_cta - 1) / per_cta;
+    if (grid > 0x7fffffffULL) return cudaErrorInvalidConfiguration;
+    k_stage_from_host<<<unsigned(grid), kThreads, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                                           n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_offload_gather(const void *host_k, const void *host_v, const int32_t *page_table, int B,
                                   int n_host_pages, const Shape &s, void *pool_k, void *pool_v,

@@ -335,6 +335,39 @@ msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int3
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_lse_merge");
 }
 
+// The device address of page-locked host memory (cudaHostAlloc, cudaMallocHost or
+// cudaHostRegister), or nullptr for anything else.  Pageable memory is addressable by the GPU
+// on some systems (address translation over the host link) but not on all, and the driver's
+// host-pointer lookup accepts it there, so the memory type is checked instead.
+static void *pinned_device_ptr(const void *p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Decode results (out, lse) may live in device memory or in page-locked host memory; in the
+// latter case the attention kernel writes them straight into it over the host link.  *dev gets
+// the address the kernel writes through; anything else is refused.
+static msa_status_t result_ptr(void *p, void **dev, const char *who) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MSA_ERR_INVALID_ARG, "%s: out and lse must be device or page-locked host memory", who);
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dev = p;
+        return MSA_OK;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        *dev = a.devicePointer;
+        return MSA_OK;
+    }
+    return fail(MSA_ERR_INVALID_ARG, "%s: out and lse must be device or page-locked host memory", who);
+}
+
 msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const void *v_cache,
                                     const int32_t *page_table, const int32_t *row_len, int32_t B, int32_t n_pages,
                                     const msa_dims_t *dims, void *out, float *lse, void *workspace,
@@ -352,8 +385,12 @@ msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const vo
         return fail(MSA_ERR_WORKSPACE, "msa_sparse_attn_decode: workspace needs %zu bytes", need);
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
         return fail(MSA_ERR_INVALID_ARG, "msa_sparse_attn_decode: caches must be 16-byte aligned");
-    cudaError_t e = launch_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, s, out, lse, workspace,
-                                       err_word, static_cast<cudaStream_t>(stream));
+    void *out_d = nullptr, *lse_d = nullptr;
+    if ((st = result_ptr(out, &out_d, "msa_sparse_attn_decode")) != MSA_OK) return st;
+    if ((st = result_ptr(lse, &lse_d, "msa_sparse_attn_decode")) != MSA_OK) return st;
+    cudaError_t e = launch_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, s, out_d,
+                                       static_cast<float *>(lse_d), workspace, err_word,
+                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_attn_decode");
 }
 
@@ -371,15 +408,29 @@ msa_status_t msa_offload_gather(const void *host_k_cache, const void *host_v_cac
          reinterpret_cast<uintptr_t>(pool_k) | reinterpret_cast<uintptr_t>(pool_v)) & 15u)
         return fail(MSA_ERR_INVALID_ARG, "msa_offload_gather: caches and pools must be 16-byte aligned");
     // the GPU reads the host caches in place: they must be page-locked and mapped
-    void *dk = nullptr, *dv = nullptr;
-    if (cudaHostGetDevicePointer(&dk, const_cast<void *>(host_k_cache), 0) != cudaSuccess ||
-        cudaHostGetDevicePointer(&dv, const_cast<void *>(host_v_cache), 0) != cudaSuccess) {
-        cudaGetLastError();
-        return fail(MSA_ERR_INVALID_ARG, "msa_offload_gather: host caches must be page-locked host memory");
-    }
+    void *dk = pinned_device_ptr(host_k_cache), *dv = pinned_device_ptr(host_v_cache);
+    if (!dk || !dv) return fail(MSA_ERR_INVALID_ARG, "msa_offload_gather: host caches must be page-locked host memory");
     cudaError_t e = launch_offload_gather(dk, dv, page_table, B, n_host_pages, s, pool_k, pool_v, pool_page_table,
                                           err_word, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_offload_gather");
+}
+
+msa_status_t msa_stage_from_host(const void *host_src, void *dev_dst, size_t bytes, msa_stream_t stream) {
+    if (bytes == 0) return MSA_OK;
+    MSA_REQUIRE(host_src && dev_dst, "msa_stage_from_host: NULL pointer");
+    if (((reinterpret_cast<uintptr_t>(host_src) | reinterpret_cast<uintptr_t>(dev_dst)) & 15u) || (bytes & 15u))
+        return fail(MSA_ERR_INVALID_ARG, "msa_stage_from_host: pointers and size must be multiples of 16 bytes");
+    // the kernel reads the host buffer in place: it must be page-locked and mapped
+    void *src = pinned_device_ptr(host_src);
+    if (!src) return fail(MSA_ERR_INVALID_ARG, "msa_stage_from_host: the source must be page-locked host memory");
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, dev_dst) != cudaSuccess ||
+        (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)) {
+        cudaGetLastError();
+        return fail(MSA_ERR_INVALID_ARG, "msa_stage_from_host: the destination must be device memory");
+    }
+    const cudaError_t e = launch_stage_from_host(src, dev_dst, bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_stage_from_host");
 }
 
 msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cache, const void *v_cache,
@@ -402,6 +453,9 @@ msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cac
         return fail(MSA_ERR_WORKSPACE, "msa_decode_step: workspace needs %zu bytes", need);
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15u)
         return fail(MSA_ERR_INVALID_ARG, "msa_decode_step: caches must be 16-byte aligned");
+    void *out_d = nullptr, *lse_d = nullptr;
+    if ((st = result_ptr(out, &out_d, "msa_decode_step")) != MSA_OK) return st;
+    if ((st = result_ptr(lse, &lse_d, "msa_decode_step")) != MSA_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_score_decode_seq(q_idx, kidx_cache, block_table, seq_lens, B, n_pages, s, scores,
                                             err_word, cs);
@@ -410,8 +464,8 @@ msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cac
     e = launch_decode_select(scores, seq_lens, block_table, B, n_pages, s, sel, page_table, row_len, counters,
                              err_word, cs, true);
     if (e != cudaSuccess) return cuda_fail(e, "msa_decode_step (selection)");
-    e = launch_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, s, out, lse, workspace, err_word,
-                           cs, true, true);
+    e = launch_attn_decode(q, k_cache, v_cache, page_table, row_len, B, n_pages, s, out_d, static_cast<float *>(lse_d),
+                           workspace, err_word, cs, true, true);
     return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_decode_step (attention)");
 }
 

@@ -40,6 +40,8 @@ cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32
                                 int n_pages, const Shape &s, float *scores, int32_t *err,
                                 cudaStream_t st);
 
+// `bytes` (a multiple of 16) from page-locked host memory (its device mapping) to device memory.
+cudaError_t launch_stage_from_host(const void *src, void *dst, size_t bytes, cudaStream_t st);
 // Selected K/V pages from host memory into a device pool (zero-copy gather).
 cudaError_t launch_offload_gather(const void *host_k, const void *host_v, const int32_t *page_table, int B,
                                   int n_host_pages, const Shape &s, void *pool_k, void *pool_v,

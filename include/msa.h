@@ -14,8 +14,10 @@
  *           (news.ainew.jp) -- MSA paragraph after Table 1 (each KV block read once).
  *
  * Conventions for every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller; the library
- *     allocates no memory.  bf16 tensors are passed as `const void *` and hold
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except where
+ *     an entry point says that page-locked host memory is accepted (the host
+ *     caches of msa_offload_gather, the source of msa_stage_from_host, out and
+ *     lse of the decode attention); the library allocates no memory.  bf16 tensors are passed as `const void *` and hold
  *     IEEE bfloat16 bit patterns.  All tensors are dense, row-major, with the
  *     shapes written beside each argument.
  *   - Paged caches share one page pool of n_pages pages of page_size = 128
@@ -289,7 +291,9 @@ msa_status_t msa_lse_merge(const void *o_part, const float *lse_part, const int3
  *
  *   q          bf16 [B][Hq][D]
  *   page_table int32 [B*G][topk];  row_len int32 [B*G]
- *   out        bf16 [B][Hq][D]  out;  lse fp32 [B][Hq]  out
+ *   out        bf16 [B][Hq][D]  out;  lse fp32 [B][Hq]  out: device memory or
+ *              page-locked host memory, written directly over the host link
+ *              (other host memory gives MSA_ERR_INVALID_ARG)
  *   workspace  device scratch of msa_workspace_bytes(MSA_OP_DECODE, B, ...) bytes
  */
 msa_status_t msa_sparse_attn_decode(const void *q, const void *k_cache, const void *v_cache,
@@ -324,6 +328,24 @@ msa_status_t msa_offload_gather(const void *host_k_cache, const void *host_v_cac
                                 void *pool_v, int32_t *pool_page_table, int32_t *err_word, msa_stream_t stream);
 
 /*
+ * msa_stage_from_host -- copy a step's packed inputs from page-locked host memory
+ * to device memory.  Not an MSA operation: the transport of a decode step's
+ * per-step inputs (q, q_idx, seq_lens, block table; a few hundred KB), done by a
+ * kernel whose 16-byte loads read the host buffer in place over the host link
+ * instead of by a copy-engine transfer, whose fixed cost (about 10 us on a
+ * Grace-Blackwell node) exceeds the transfer itself at this size.
+ *   host_src  page-locked host memory (cudaHostAlloc, cudaMallocHost or
+ *             cudaHostRegister), 16-byte aligned
+ *   dev_dst   device memory, 16-byte aligned
+ *   bytes     a multiple of 16
+ * Ordered on `stream` like a cudaMemcpyAsync; the host buffer must not change
+ * until the copy has run.  Errors: MSA_ERR_INVALID_ARG for a source that is not
+ * page-locked host memory, a destination that is not device memory, or a
+ * pointer or size that is not a multiple of 16 bytes.
+ */
+msa_status_t msa_stage_from_host(const void *host_src, void *dev_dst, size_t bytes, msa_stream_t stream);
+
+/*
  * msa_decode_step -- one whole decode step for B requests, each with one new
  * query token at position seq_lens[b] - 1: index scan (msa_index_score,
  * MSA_PHASE_DECODE, rows = requests), top-k (msa_topk_blocks), page tables
@@ -339,9 +361,12 @@ msa_status_t msa_offload_gather(const void *host_k_cache, const void *host_v_cac
  *   scores      fp32 [B][G][max_blocks]  out
  *   sel         int32 [B][G][topk]       out
  *   page_table  int32 [B*G][topk], row_len int32 [B*G]  out
- *   out         bf16 [B][Hq][D], lse fp32 [B][Hq]      out
+ *   out         bf16 [B][Hq][D], lse fp32 [B][Hq]      out: device memory or
+ *               page-locked host memory, which the attention kernel then writes
+ *               directly over the host link (no separate copy of the results)
  *   workspace   msa_workspace_bytes(MSA_OP_DECODE, B, 0, dims) bytes
- * Limits: B*G <= 65535, max_blocks <= 16384; caches 16-byte aligned.
+ * Limits: B*G <= 65535, max_blocks <= 16384; caches 16-byte aligned.  out or lse
+ * in other host memory gives MSA_ERR_INVALID_ARG.
  */
 msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cache, const void *v_cache,
                              const void *kidx_cache, const int32_t *block_table, const int32_t *seq_lens, int32_t B,

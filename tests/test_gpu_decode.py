@@ -151,8 +151,9 @@ def test_out_of_range_page_is_flagged(msa):
 
 
 def test_packed_inputs_and_results(msa):
-    """DecodeInputs (one host-to-device copy of all step inputs) and DecodeStep.download
-    (one copy of out and lse) give the same bits as the step on separate tensors."""
+    """DecodeInputs (one staging kernel for all step inputs), DecodeStep.download (one copy
+    of out and lse) and a step writing out and lse into page-locked host memory give the
+    same bits as the step on separate device tensors."""
     case = mi.decode_case([700, 3000, 129], Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=80, needles_per_group=2,
                           seed=11, device=DEV)
     dims = msa.dims_of(case)
@@ -173,6 +174,39 @@ def test_packed_inputs_and_results(msa):
     torch.cuda.synchronize()
     msa.msa_check(step.err)
     assert torch.equal(h_out, ref_out) and torch.equal(h_lse, ref_lse)
+    # the step writing out and lse straight into page-locked host memory gives the same bits
+    _, (z_out, z_lse) = step.host_results()
+    step(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table, inputs.seq_lens,
+         inputs.q_pos, out=z_out, lse=z_lse)
+    torch.cuda.synchronize()
+    msa.msa_check(step.err)
+    assert torch.equal(z_out, ref_out) and torch.equal(z_lse, ref_lse)
+    with pytest.raises(ValueError):   # pageable host memory is refused
+        step(inputs.q, inputs.q_idx, case.k_cache, case.v_cache, case.kidx_cache, inputs.block_table,
+             inputs.seq_lens, inputs.q_pos, out=torch.empty_like(z_out), lse=z_lse)
+
+
+def test_stage_from_host(msa):
+    """msa_stage_from_host copies page-locked host bytes into device memory exactly (a size
+    that ends inside a CTA's share too), and refuses, on the host, a source that is not
+    page-locked host memory or a size that is not a multiple of 16 bytes."""
+    import ctypes
+    gen = torch.Generator().manual_seed(5)
+    for n in (16, 4096 * 16 + 48, 155 * 1024):
+        host = torch.randint(0, 256, (n,), generator=gen, dtype=torch.uint8).pin_memory()
+        dev = torch.zeros(n, dtype=torch.uint8, device=DEV)
+        msa.msa_stage_from_host(host, dev)
+        torch.cuda.synchronize()
+        assert torch.equal(dev.cpu(), host)
+    lib, dev = msa.library(), torch.zeros(64, dtype=torch.uint8, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    pageable = torch.zeros(64, dtype=torch.uint8)
+    pinned = torch.zeros(64, dtype=torch.uint8).pin_memory()
+    for src, nbytes in ((pageable, 64), (dev, 64), (pinned, 40)):
+        rc = lib.msa_stage_from_host(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dev.data_ptr()), nbytes, stream)
+        assert rc == 1, (src.device, nbytes, rc)   # MSA_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        msa.msa_stage_from_host(pageable, dev)
 
 
 def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(msa):
@@ -190,9 +224,9 @@ def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(msa):
 
 def test_decode_step_graph_replay(msa):
     """DecodeStep.capture() records the whole step (and, with DecodeInputs and a host
-    result buffer, its upload and download) into a CUDA graph; replay() gives the same
-    bits as the eager step, and new inputs written into the captured tensors are picked
-    up by the next replay."""
+    result buffer, its upload and its results written into host memory) into a CUDA
+    graph; replay() gives the same bits as the eager step, and new inputs written into
+    the captured tensors are picked up by the next replay."""
     case = mi.decode_case([700, 3000, 129, 60000], Hq=64, G=8, D=128, Di=64, topk=16, pool_pages=600,
                           needles_per_group=2, seed=19, device=DEV)
     dims = msa.dims_of(case)
@@ -216,6 +250,7 @@ def test_decode_step_graph_replay(msa):
               case.block_table, case.seq_lens)
         msa.msa_check(eager.err)
         torch.cuda.synchronize()
-        for name in ("sel", "page_table", "row_len", "out", "lse"):
+        for name in ("sel", "page_table", "row_len"):
             assert torch.equal(getattr(step, name), getattr(eager, name)), (it, name)
+        # the captured step writes out and lse into the page-locked host buffer
         assert torch.equal(h_out, eager.out.cpu()) and torch.equal(h_lse, eager.lse.cpu()), it

@@ -77,3 +77,11 @@ def test_offload_rejects_unpinned_host_cache(msa):
     pt = torch.full((8, 8), -1, dtype=torch.int32, device=DEV)
     with pytest.raises(ValueError, match="page-locked"):
         msa.msa_offload_gather(case.k_cache.cpu(), case.v_cache.cpu(), pt, dims)
+    # the C entry point itself refuses pageable memory, also where the GPU could address it
+    import ctypes
+    k, v = case.k_cache.cpu(), case.v_cache.cpu()
+    scratch, err = torch.empty(16, dtype=torch.uint8, device=DEV), msa.new_err_word(DEV)
+    d, P = dims.c(), lambda t: ctypes.c_void_p(t.data_ptr())
+    rc = msa.library().msa_offload_gather(P(k), P(v), k.shape[0], P(pt), 1, ctypes.byref(d), P(scratch), P(scratch),
+                                          P(pt), P(err), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 1   # MSA_ERR_INVALID_ARG
