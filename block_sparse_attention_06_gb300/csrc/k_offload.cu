@@ -71,6 +71,7 @@ constexpr int kStagePer = 4;   // 16-byte pieces per thread
 
 __global__ void __launch_bounds__(kThreads) k_stage_from_host(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                                                               size_t n) {
+    pdl_trigger();   // a decode step's scan may start launching; it waits for this kernel to complete
     const size_t base = size_t(blockIdx.x) * kThreads * kStagePer + threadIdx.x;
     uint4 v[kStagePer];
 #pragma unroll

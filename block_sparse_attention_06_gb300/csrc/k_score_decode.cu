@@ -34,6 +34,9 @@ __global__ void __launch_bounds__(256) k_score_decode(
     const int tid = threadIdx.x;
     float *out = scores + size_t(r) * G * max_blocks + j;
 
+    // In a decode step the scan may be a programmatic dependent of the kernel that staged its
+    // inputs: nothing is read before that kernel completes.  Launched plainly, this returns at once.
+    pdl_wait();
     pdl_trigger();   // the selection kernel may start launching once every scan CTA runs
 
     // rows are either (q_req, q_pos) pairs or the requests themselves at seq_lens - 1
@@ -101,25 +104,24 @@ __global__ void __launch_bounds__(256) k_score_decode(
 template <int G, int DI>
 cudaError_t launch_g(const void *q_idx, const void *kidx, const int32_t *bt, const int32_t *q_req,
                      const int32_t *q_pos, const int32_t *seq_lens, int n_rows, int n_req, int n_pages,
-                     int max_blocks, float *scores, int32_t *err, cudaStream_t st) {
+                     int max_blocks, float *scores, int32_t *err, cudaStream_t st, bool pdl) {
     const long long grid = 1LL * n_rows * max_blocks;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    k_score_decode<G, DI><<<unsigned(grid), 256, 0, st>>>(
-        static_cast<const uint16_t *>(q_idx), static_cast<const uint8_t *>(kidx), bt, q_req, q_pos, seq_lens,
-        n_req, n_pages, max_blocks, scores, err);
-    return cudaGetLastError();
+    return launch_kernel(k_score_decode<G, DI>, dim3(unsigned(grid)), dim3(256), 0, st, pdl,
+                         static_cast<const uint16_t *>(q_idx), static_cast<const uint8_t *>(kidx), bt, q_req, q_pos,
+                         seq_lens, n_req, n_pages, max_blocks, scores, err);
 }
 
 }  // namespace
 
 static cudaError_t launch_any(const void *q_idx, const void *kidx, const int32_t *block_table, const int32_t *q_req,
                               const int32_t *q_pos, const int32_t *seq_lens, int n_rows, int n_req, int n_pages,
-                              const Shape &s, float *scores, int32_t *err, cudaStream_t st) {
+                              const Shape &s, float *scores, int32_t *err, cudaStream_t st, bool pdl) {
 #define MSA_SD_CASE(GG, DD)                                                                               \
     if (s.G == GG && s.Di == DD)                                                                          \
         return launch_g<GG, DD>(q_idx, kidx, block_table, q_req, q_pos, seq_lens, n_rows, n_req, n_pages, \
-                                s.max_blocks, scores, err, st);
+                                s.max_blocks, scores, err, st, pdl);
     MSA_SD_CASE(1, 32) MSA_SD_CASE(1, 64) MSA_SD_CASE(2, 32) MSA_SD_CASE(2, 64)
     MSA_SD_CASE(4, 32) MSA_SD_CASE(4, 64) MSA_SD_CASE(8, 32) MSA_SD_CASE(8, 64)
     MSA_SD_CASE(16, 32) MSA_SD_CASE(16, 64)
@@ -131,13 +133,14 @@ cudaError_t launch_score_decode(const void *q_idx, const void *kidx, const int32
                                 const int32_t *q_req, const int32_t *q_pos, int n_rows, int n_req,
                                 int n_pages, const Shape &s, float *scores, int32_t *err,
                                 cudaStream_t st) {
-    return launch_any(q_idx, kidx, block_table, q_req, q_pos, nullptr, n_rows, n_req, n_pages, s, scores, err, st);
+    return launch_any(q_idx, kidx, block_table, q_req, q_pos, nullptr, n_rows, n_req, n_pages, s, scores, err, st,
+                      false);
 }
 
 cudaError_t launch_score_decode_seq(const void *q_idx, const void *kidx, const int32_t *block_table,
                                     const int32_t *seq_lens, int B, int n_pages, const Shape &s,
-                                    float *scores, int32_t *err, cudaStream_t st) {
-    return launch_any(q_idx, kidx, block_table, nullptr, nullptr, seq_lens, B, B, n_pages, s, scores, err, st);
+                                    float *scores, int32_t *err, cudaStream_t st, bool pdl) {
+    return launch_any(q_idx, kidx, block_table, nullptr, nullptr, seq_lens, B, B, n_pages, s, scores, err, st, pdl);
 }
 
 }  // namespace msa

@@ -457,8 +457,10 @@ msa_status_t msa_decode_step(const void *q, const void *q_idx, const void *k_cac
     if ((st = result_ptr(out, &out_d, "msa_decode_step")) != MSA_OK) return st;
     if ((st = result_ptr(lse, &lse_d, "msa_decode_step")) != MSA_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // the scan may start while the kernel before it on the stream (say, the one staging this step's
+    // inputs) drains; it reads nothing until that kernel completes
     cudaError_t e = launch_score_decode_seq(q_idx, kidx_cache, block_table, seq_lens, B, n_pages, s, scores,
-                                            err_word, cs);
+                                            err_word, cs, true);
     if (e != cudaSuccess) return cuda_fail(e, "msa_decode_step (index scan)");
     int32_t *counters = decode_ws_counters(workspace, B, s);
     e = launch_decode_select(scores, seq_lens, block_table, B, n_pages, s, sel, page_table, row_len, counters,

@@ -127,7 +127,7 @@ cudaError_t launch_decode_select(const float *scores, const int32_t *seq_lens, c
 // b at position seq_lens[b] - 1).
 cudaError_t launch_score_decode_seq(const void *q_idx, const void *kidx, const int32_t *block_table,
                                     const int32_t *seq_lens, int B, int n_pages, const Shape &s,
-                                    float *scores, int32_t *err, cudaStream_t st);
+                                    float *scores, int32_t *err, cudaStream_t st, bool pdl = false);
 
 // Tensor-map creation through the driver entry point (no libcuda link dependency).
 bool encode_tensor_map(void *map, int rank, const void *base, const uint64_t *dims,
