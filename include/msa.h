@@ -353,7 +353,9 @@ msa_status_t msa_stage_from_host(const void *host_src, void *dev_dst, size_t byt
  * with the same results as those four calls.  [T-zh 解码索引评分内核优化,
  * 将 MSA 与分页注意力集成]; [T-zh 未来工作]: the small top-k and page-table kernels
  * are fused into one.  Three kernels run back to back with programmatic
- * dependent launch, so each starts while the previous one drains.
+ * dependent launch, so each starts while the previous one drains; the scan is
+ * launched that way too and reads nothing before the kernel ahead of it on the
+ * stream has completed.
  *
  *   q           bf16 [B][Hq][D];  q_idx bf16 [B][G][Di]
  *   k_cache, v_cache bf16 [n_pages][128][G][D];  kidx_cache bf16 [n_pages][128][G][Di]
