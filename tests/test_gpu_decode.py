@@ -124,8 +124,9 @@ def test_decode1m(msa):
 @pytest.mark.parametrize("blocks", [150, 901, 1800, 3001, 10000])
 def test_decode_selection_tiers(msa, blocks):
     """The decode selection kernel's launch shapes by context length: a CTA per (request,
-    group) row of 256 threads (up to 256 blocks), then 512 threads holding 2, 4, 8 or 32
-    candidates each; a short request shares every batch."""
+    group) row of 256 or 1,024 threads with one candidate each (up to 256 / 1,024 blocks),
+    then 512 threads holding 4, 8 or 32 candidates each; a short request shares every
+    batch."""
     lens = [blocks * 128 - 37, 3000]
     case = mi.decode_case(lens, Hq=8, G=2, D=64, Di=32, topk=16, pool_pages=blocks + 40, needles_per_group=3,
                           seed=600 + blocks, device=DEV)
