@@ -29,7 +29,12 @@
 //              with busy warps feeds the tensor core at a fraction of its rate:
 //              sub-partition 1 holds only this warp and one warp of each softmax
 //              group and of the epilogue (those must cover all four TMEM lane
-//              quarters), and each group of MMAs is issued from one asm block;
+//              quarters), and each group of MMAs is issued from one asm block.
+//              The tensor core takes an MMA about when the one before it ends, so
+//              the issuer's own waits are idle tensor time: per tile it waits on
+//              the Q buffer (whose loader has read the tile's descriptor first, so
+//              the flags can be read after it), on one barrier for the previous
+//              tile's P and O buffer together, and on K or V at a chunk's start;
 //   warp 2     K/V loader: K_j by TMA (128B swizzle, 64-column boxes) once the
 //              previous chunk's last S has completed, V_j once its last PV has;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
@@ -98,7 +103,8 @@ struct AttnSmem {
     int32_t chunk_page[4], chunk_g[4];              // decoder -> K/V loader
     uint64_t k_full, k_empty, v_full, v_empty;
     uint64_t q_full[kQBuf], q_empty[kQBuf];
-    uint64_t s_full[2], p_full[2], o_full[2], o_free[2];
+    uint64_t s_full[2], o_full[2];
+    uint64_t pv_ready[2];   // P written by the tile's softmax group and its O buffer read out by the epilogue
     uint64_t stat_full[4], stat_free[4];            // inv_le[i] written / read by the epilogue
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
@@ -206,6 +212,10 @@ __device__ __forceinline__ void mma_pv_block(uint32_t d, uint32_t a, uint64_t b,
         : "memory");
 }
 
+__device__ __forceinline__ int sm_flags(const TileDesc &d) {
+    return *reinterpret_cast<const volatile int32_t *>(&d.flags);
+}
+
 // Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
 constexpr size_t kPlanHeaderBytes = 16;
 
@@ -306,9 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         mbar_init(&sm.k_empty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);
-            mbar_init(&sm.p_full[b], 4);
+            mbar_init(&sm.pv_ready[b], 8);   // 4 softmax warps (P) + 4 epilogue warps (O two tiles back)
             mbar_init(&sm.o_full[b], 1);
-            mbar_init(&sm.o_free[b], 4);
         }
         mbar_init(&sm.v_full, 1);
         mbar_init(&sm.v_empty, 1);
@@ -327,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         }
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
+        for (int b = 0; b < 2; ++b)   // the first tile of each O buffer has no earlier tile to read out
+            for (int i = 0; i < 4; ++i) mbar_arrive(&sm.pv_ready[b]);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -506,16 +517,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         // ------------------------------------------------------------ MMA issuer (lane 0)
         // The warp shares its sub-partition with busy softmax and epilogue warps, and every issue
         // slot it needs per MMA slows the tensor core down: each group of MMAs is one asm block.
+        // Every MMA is accepted about when the one before it finishes, so a wait of this thread between
+        // two MMA groups leaves the tensor core idle: a tile costs the issuer three waits (its Q,
+        // which also publishes its descriptor; the previous tile's P and O buffer, one barrier; K or V
+        // on a chunk's first tile) and one read of its flags.
         if (lane == 0) {
-            int u = 0, cs_k = -1, cs_v = -1;
-            bool have_prev = false;
             const uint64_t kd = make_smem_desc(smem_u32(sm.k), 16, 1024, 2);
             const uint64_t vd = make_smem_desc(smem_u32(sm.v), 16384, 1024, 2);
-            int p_u = 0, p_flags = 0;
-            auto do_pv = [&](int t, int flags) -> bool {
+            int cs_k = -1, cs_v = -1;
+            auto issue_pv = [&](int t, int flags) -> bool {
                 const int b = t & 1;
-                if (!mbar_wait(&sm.p_full[b], (t >> 1) & 1, err, &sm.abort)) return false;
-                if (t >= 2 && !mbar_wait(&sm.o_free[b], ((t >> 1) - 1) & 1, err, &sm.abort)) return false;
+                if (!mbar_wait(&sm.pv_ready[b], (t >> 1) & 1, err, &sm.abort)) return false;
                 if (flags & kFlagFirst) {
                     ++cs_v;
                     if (!mbar_wait(&sm.v_full, cs_v & 1, err, &sm.abort)) return false;
@@ -526,18 +538,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 if (flags & kFlagLast) mma_commit(&sm.v_empty);
                 return true;
             };
-            for (;;) {
+            int pu = -1, pflags = 0;   // the tile whose PV is pending (issued after the next tile's S)
+            for (int u = 0;; ++u) {
+                // the Q loader reads the tile's descriptor before it loads Q (an end marker completes
+                // the phase with no bytes), so a full Q buffer means the flags can be read
+                const int qb = u % kQBuf;
+                if (!mbar_wait(&sm.q_full[qb], (u / kQBuf) & 1, err, &sm.abort)) break;
                 const int slot = u % kRing;
-                if (!mbar_wait(&sm.desc_full[slot], (u / kRing) & 1, err, &sm.abort)) break;
-                const int flags = *reinterpret_cast<volatile int32_t *>(&sm.desc[slot].flags);
+                const int flags = sm_flags(sm.desc[slot]);
                 if (flags & kFlagEnd) break;
                 mbar_arrive(&sm.desc_empty[slot]);
                 if (flags & kFlagFirst) {
                     ++cs_k;
                     if (!mbar_wait(&sm.k_full, cs_k & 1, err, &sm.abort)) break;
                 }
-                const int qb = u % kQBuf;
-                if (!mbar_wait(&sm.q_full[qb], (u / kQBuf) & 1, err, &sm.abort)) break;
                 tc_fence_after();
                 const int b = u & 1;
                 mma_s_block<D / 16>(tmem + uint32_t(b * 128), make_smem_desc(smem_u32(sm.q[qb]), 16, 1024, 2), kd,
@@ -545,16 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 mma_commit(&sm.s_full[b]);
                 mma_commit(&sm.q_empty[qb]);
                 if (flags & kFlagLast) mma_commit(&sm.k_empty);
-                if (have_prev && !do_pv(p_u, p_flags)) {
-                    have_prev = false;
+                if (pu >= 0 && !issue_pv(pu, pflags)) {
+                    pu = -1;
                     break;
                 }
-                have_prev = true;
-                p_u = u;
-                p_flags = flags;
-                ++u;
+                pu = u;
+                pflags = flags;
             }
-            if (have_prev && !sm.abort) do_pv(p_u, p_flags);
+            if (pu >= 0 && !sm.abort) issue_pv(pu, pflags);
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, err, nullptr);
         }
@@ -576,7 +588,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const volatile TileDesc &d = sm.desc[slot];
             if (d.flags & kFlagEnd) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.desc_full[slot]);
+                // the MMA issuer learns of the end through this tile's Q barrier: its phase completes
+                // (with no bytes) once the buffer's previous tile has been consumed
+                if (lane == 0) {
+                    mbar_arrive(&sm.desc_full[slot]);
+                    if (u < kQBuf || mbar_wait(&sm.q_empty[qb], ((u / kQBuf) - 1) & 1, err, &sm.abort))
+                        mbar_arrive(&sm.q_full[qb]);
+                }
                 break;
             }
             if (u >= kQBuf &&
@@ -730,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sm.stat_full[u & 3]);
-                mbar_arrive(&sm.p_full[wg]);
+                mbar_arrive(&sm.pv_ready[wg]);
             }
             float lg;
             asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(le));
@@ -789,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             fence_proxy_async_smem();   // the staged rows are read by the TMA engine
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&sm.o_free[b]);
+                mbar_arrive(&sm.pv_ready[b]);
                 // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 of the CSR-ordered partials are one contiguous
                 // block; this warp's rows quad*32 .. quad*32+31 of it leave in power-of-two boxes (32, 16,
                 // 8, 4 rows; each starts on an 8-row, 1024-byte boundary of the swizzled staging layout)
