@@ -332,6 +332,24 @@ def msa_invert_selection(sel, q_req, n_req: int, dims: Dims, blk_off=None, blk_e
     return blk_off, blk_ent, ent_pos
 
 
+def partials_shape(n_ent: int, hpg: int, D: int):
+    """Shape of the prefill partials buffer: per entry, D // 8 column chunks x hpg heads x 8 bf16
+    (the layout msa.h documents)."""
+    return (n_ent, D // 8, hpg, 8)
+
+
+def partials_entry_major(o_part, n_ent: int, hpg: int, D: int):
+    """The partials rearranged as [n_ent][hpg][D] (a permute; for inspection and tests)."""
+    return o_part[:n_ent].permute(0, 2, 1, 3).reshape(n_ent, hpg, D)
+
+
+def partials_from_entry_major(o_ent, hpg: int, D: int):
+    """[n_ent][hpg][D] partials rearranged into the prefill partials layout (the inverse of
+    partials_entry_major)."""
+    n_ent = o_ent.shape[0]
+    return o_ent.reshape(n_ent, hpg, D // 8, 8).permute(0, 2, 1, 3).contiguous()
+
+
 def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_off, blk_ent, dims: Dims,
                             o_part=None, lse_part=None, workspace=None, err_word=None):
     n_rows = q.shape[0]
@@ -349,10 +367,10 @@ def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_
     dev = q.device
     n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
     if o_part is None:
-        o_part = torch.empty((n_ent, hpg, dims.D), dtype=torch.bfloat16, device=dev)
+        o_part = torch.empty(partials_shape(n_ent, hpg, dims.D), dtype=torch.bfloat16, device=dev)
     if lse_part is None:
         lse_part = torch.empty((n_ent, hpg), dtype=torch.float32, device=dev)
-    _req(o_part, torch.bfloat16, "o_part", (n_ent, hpg, dims.D))
+    _req(o_part, torch.bfloat16, "o_part", partials_shape(n_ent, hpg, dims.D))
     _req(lse_part, torch.float32, "lse_part", (n_ent, hpg))
     need = msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)
     if workspace is None:
@@ -369,7 +387,7 @@ def msa_sparse_attn_prefill(q, k_cache, v_cache, block_table, q_req, q_pos, blk_
 def msa_lse_merge(o_part, lse_part, sel, ent_pos, dims: Dims, out=None, lse=None, err_word=None):
     n_rows = sel.shape[0]
     n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
-    _req(o_part, torch.bfloat16, "o_part", (n_ent, hpg, dims.D))
+    _req(o_part, torch.bfloat16, "o_part", partials_shape(n_ent, hpg, dims.D))
     _req(lse_part, torch.float32, "lse_part", (n_ent, hpg))
     _req(sel, torch.int32, "sel", (n_rows, dims.G, dims.topk))
     _req(ent_pos, torch.int32, "ent_pos", (n_rows, dims.G, dims.topk))
@@ -712,7 +730,7 @@ class PrefillStep:
         self.attn_ws = torch.empty((max(1, msa_workspace_bytes(MSA_OP_PREFILL, n_rows, n_req, dims)),),
                                    dtype=torch.uint8, **f)
         n_ent, hpg = n_rows * dims.G * dims.topk, dims.Hq // dims.G
-        self.o_part = torch.empty((n_ent, hpg, dims.D), dtype=torch.bfloat16, **f)
+        self.o_part = torch.empty(partials_shape(n_ent, hpg, dims.D), dtype=torch.bfloat16, **f)
         self.lse_part = torch.empty((n_ent, hpg), dtype=torch.float32, **f)
         self.out = torch.empty((n_rows, dims.Hq, dims.D), dtype=torch.bfloat16, **f)
         self.lse = torch.empty((n_rows, dims.Hq), dtype=torch.float32, **f)
@@ -744,7 +762,7 @@ class PrefillStep:
         sel, pos = self.sel.cpu(), self.ent_pos.cpu()
         n_rows, G, k = sel.shape
         hpg = self.dims.Hq // G
-        op = self.o_part.cpu()
+        op = partials_entry_major(self.o_part.cpu(), n_rows * G * k, hpg, self.dims.D)
         lp = self.lse_part.cpu()
         valid = sel >= 0
         p = torch.where(valid, pos, torch.zeros_like(pos)).long()

@@ -44,12 +44,13 @@
 //              read the previous one) and its lse to the partials; while one group
 //              runs its softmax the tensor core works on the other group's tile;
 //   warps 12-15  epilogue: every tile in order, O chunk by chunk from TMEM,
-//              normalised, into the shared staging buffer in the 128B-swizzled
-//              box layout, so a softmax group goes on to its next tile as soon
-//              as its P is in TMEM.  A staged tile is one contiguous block of the
-//              CSR-ordered partials; each warp stages its own 32 rows and sends
-//              them by TMA bulk tensor stores in a few power-of-two row boxes, so
-//              no warp waits for another to reuse the staging buffer;
+//              normalised, and stored from registers, so a softmax group goes on
+//              to its next tile as soon as its P is in TMEM.  The partials are
+//              laid out for these stores: within each entry's HPG x D block the
+//              16-byte column chunk is the outer index and the head the inner one,
+//              so the 32 rows of a warp (4 entries x 8 heads, or 8 x 4), one per
+//              lane, write whole 128-byte lines per store instruction.  No staging
+//              buffer, no TMA store, and no shared-memory traffic for the output;
 //   warp 17    idle (it would share the MMA warp's sub-partition);
 //   warps 16, 3, 18  Q loaders, one per Q buffer, one tile each in turn: the HPG
 //              heads of each entry's query row (HPG * D * 2 contiguous bytes) in
@@ -74,7 +75,6 @@ constexpr int kThreads = 608;
 constexpr int kChunkTiles = 8;   // tiles per work chunk
 constexpr int kRing = 16;        // tile descriptors in flight (two chunks)
 constexpr int kQBuf = 3;         // Q buffers
-constexpr int kStoreBoxes = 6;   // store boxes of 128, 64, 32, 16, 8, 4 rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -97,7 +97,6 @@ struct AttnSmem {
     alignas(1024) uint8_t k[D * 128 * 2];
     alignas(1024) uint8_t v[D * 128 * 2];
     alignas(1024) uint8_t q[kQBuf][128 * D * 2];
-    alignas(1024) uint8_t stg[128 * D * 2];         // one tile's bf16 output on its way to the partials
     TileDesc desc[kRing];
     float inv_le[4][128];                           // 1 / row sum of P, per tile mod 4 (softmax -> epilogue)
     int32_t chunk_page[4], chunk_g[4];              // decoder -> K/V loader
@@ -212,6 +211,13 @@ __device__ __forceinline__ void mma_pv_block(uint32_t d, uint32_t a, uint64_t b,
         : "memory");
 }
 
+// 16-byte global store with an L2 cache policy (l2_policy_evict_first and the like).
+__device__ __forceinline__ void st_global_v4_hint(void *p, const uint32_t (&w)[4], uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ int sm_flags(const TileDesc &d) {
     return *reinterpret_cast<const volatile int32_t *>(&d.flags);
 }
@@ -284,14 +290,10 @@ __global__ void __launch_bounds__(1024) k_attn_plan(const int32_t *__restrict__ 
 
 // ------------------------------------------------------------------ attention
 
-struct StoreMaps {
-    CUtensorMap box[kStoreBoxes];   // partials as [rows][D], boxes of 64 columns x (128 >> i) rows
-};
-
 template <int D, int HPG>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
     const uint8_t *__restrict__ qg, int Hq, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ StoreMaps omaps,
+    const __grid_constant__ CUtensorMap vmap, uint8_t *__restrict__ o_part,
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ q_req, const int32_t *__restrict__ q_pos,
     const int32_t *__restrict__ blk_off, const int32_t *__restrict__ blk_ent, int32_t *__restrict__ plan_hdr,
     const int2 *__restrict__ chunks, int n_rows, int n_req, int n_pages, int G, int topk, int max_blocks,
@@ -348,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
         tma_prefetch_desc(&vmap);
-        for (int i = 0; i < kStoreBoxes; ++i) tma_prefetch_desc(&omaps.box[i]);
     }
     tc_fence_before();
     __syncthreads();
@@ -777,9 +778,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const uint64_t inv2 = dup2(sm.inv_le[u & 3][row]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.stat_free[u & 3]);
-            // this warp's 32 staging rows are free once its stores of tile u - 1 have read them
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+            // row `row` of the tile is head h of CSR entry ent0 + row / HPG; its 16-byte chunk cc sits
+            // at byte (cc * HPG + h) * 16 of the entry's HPG x D block
+            const bool live = row < n_valid * HPG;
+            uint8_t *const gp = o_part + (size_t(ent0) + row / HPG) * (HPG * D * 2) + size_t(row % HPG) * 16;
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -788,9 +790,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    const int cc = ((c + i) >> 3) & 7;
-                    const uint32_t addr =
-                        smem_u32(sm.stg + ((c + i) >> 6) * 16384 + row * 128 + ((cc ^ (row & 7)) << 4));
                     uint32_t w4[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -798,36 +797,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                         fmul2(a, bb, __uint_as_float(o[i + 2 * j]), __uint_as_float(o[i + 2 * j + 1]), inv2);
                         w4[j] = pack_bf16x2(a, bb);
                     }
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w4[0]), "r"(w4[1]),
-                                 "r"(w4[2]), "r"(w4[3])
-                                 : "memory");
+                    if (live) st_global_v4_hint(gp + size_t((c + i) >> 3) * (HPG * 16), w4, store_policy);
                 }
             }
             tc_fence_before();
-            fence_proxy_async_smem();   // the staged rows are read by the TMA engine
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.pv_ready[b]);
-                // rows ent0*HPG .. (ent0 + n_valid)*HPG - 1 of the CSR-ordered partials are one contiguous
-                // block; this warp's rows quad*32 .. quad*32+31 of it leave in power-of-two boxes (32, 16,
-                // 8, 4 rows; each starts on an 8-row, 1024-byte boundary of the swizzled staging layout)
-                const int rows = min(32, n_valid * HPG - quad * 32);
-                int r0 = quad * 32;
-#pragma unroll
-                for (int bx = 2; bx < kStoreBoxes; ++bx) {
-                    const int R = 128 >> bx;
-                    if (rows > 0 && (rows & R)) {
-#pragma unroll
-                        for (int i = 0; i < NSUB; ++i)
-                            tma_store_2d_hint(&omaps.box[bx], sm.stg + i * 16384 + r0 * 128, i * 64,
-                                              ent0 * HPG + r0, store_policy);
-                        r0 += R;
-                    }
-                }
-                bulk_commit();
-            }
+            if (lane == 0) mbar_arrive(&sm.pv_ready[b]);   // O buffer b is free for tile u + 2
         }
-        if (lane == 0) bulk_wait_all();   // the partials are written before the CTA exits
     }
 
     tc_fence_before();
@@ -856,7 +832,6 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
                      int n_pages, const Shape &s, void *o_part, float *lse_part, void *ws, int32_t *err,
                      cudaStream_t st) {
     alignas(64) CUtensorMap qm, km, vm;
-    alignas(64) StoreMaps om;
     const char *why = nullptr;
     {
         const uint64_t dims[3] = {uint64_t(D), uint64_t(s.Hq), uint64_t(n_rows)};
@@ -871,15 +846,6 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
         if (!encode_tensor_map(&km, 4, k_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
         if (!encode_tensor_map(&vm, 4, v_cache, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
     }
-    {
-        // partials [n_rows * G * topk * HPG rows][D], row = entry * HPG + head
-        const uint64_t dims[2] = {uint64_t(D), uint64_t(n_rows) * uint64_t(s.G) * uint64_t(s.topk) * HPG};
-        const uint64_t strides[1] = {uint64_t(D) * 2};
-        for (int b = 0; b < kStoreBoxes; ++b) {
-            const uint32_t box[2] = {64u, uint32_t(128 >> b)};
-            if (!encode_tensor_map(&om.box[b], 2, o_part, dims, strides, box, 128, &why)) return cudaErrorInvalidValue;
-        }
-    }
     const long long n_keys = 1LL * s.G * n_req * s.max_blocks;
     if (n_keys > 0x7ffffffeLL) return cudaErrorInvalidConfiguration;
     const PlanLayout pl = plan_layout(n_rows, n_req, s);
@@ -893,7 +859,7 @@ cudaError_t launch_t(const void *q, const void *k_cache, const void *v_cache, co
     if (e != cudaSuccess) return e;
     return launch_kernel(k_attn_prefill<D, HPG>, dim3(unsigned(sm_count())), dim3(kThreads), smem, st, true,
                          static_cast<const uint8_t *>(q), s.Hq, qm, km,
-                         vm, om, bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows,
+                         vm, static_cast<uint8_t *>(o_part), bt, q_req, q_pos, blk_off, blk_ent, hdr, static_cast<const int2 *>(chunks), n_rows,
                          n_req, n_pages, s.G, s.topk, s.max_blocks, s.sm_scale, lse_part, err);
 }
 

@@ -4,9 +4,11 @@
 // block-major kernel only produces a partial O per KV block, a final reduction
 // based on Log-Sum-Exp rescales the partial outputs and sums them.  The partials
 // are stored in CSR-entry order (the order in which the block-major kernel
-// produces them); ent_pos maps each (row, group, slot) to its entry.  One CTA
-// per query row gathers that row's G * topk partial blocks (HPG heads x D bf16,
-// contiguous) with 16-byte loads, coalesced across a block's heads.
+// produces them); ent_pos maps each (row, group, slot) to its entry.  Within an
+// entry's HPG x D block the 16-byte column chunk is the outer index and the head
+// the inner one.  One CTA per query row gathers that row's G * topk partial blocks
+// with 16-byte loads; its threads take heads fastest, so a warp's loads for one
+// slot are contiguous (HPG heads x 32/HPG chunks).
 #include "msa_device.cuh"
 #include "msa_internal.h"
 
@@ -70,9 +72,9 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
     __syncthreads();
     const int chunks = Hq * (D / 8);
     for (int c = tid; c < chunks; c += blockDim.x) {
-        const int h = c / (D / 8);
-        const int g = h / hpg, hh = h - g * hpg;
-        const int col = (c - h * (D / 8)) * 8;
+        const int hh = c % hpg, rest = c / hpg;
+        const int cc = rest % (D / 8), g = rest / (D / 8);
+        const int h = g * hpg + hh, col = cc * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         // four slots' loads in flight at a time; an empty slot (weight 0, never written) reads
         // entry 0 instead and is left out by a select, so no stale value can reach the sum
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
                 const int s = s0 + i;
                 w[i] = s < topk ? w_s[s * Hq + h] : 0.f;
                 const int p = (s < topk && w[i] != 0.f) ? pos_s[g * topk + s] : 0;
-                v[i] = *reinterpret_cast<const uint4 *>(o_part + (size_t(p) * hpg + hh) * D + col);
+                v[i] = *reinterpret_cast<const uint4 *>(o_part + size_t(p) * hpg * D + (size_t(cc) * hpg + hh) * 8);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(256) k_lse_merge(const uint16_t *__restrict__ 
         r.y = pack_bf16x2(acc[2], acc[3]);
         r.z = pack_bf16x2(acc[4], acc[5]);
         r.w = pack_bf16x2(acc[6], acc[7]);
-        *reinterpret_cast<uint4 *>(out + size_t(q) * Hq * D + size_t(c) * 8) = r;
+        *reinterpret_cast<uint4 *>(out + (size_t(q) * Hq + h) * D + col) = r;
     }
 }
 

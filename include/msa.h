@@ -236,14 +236,22 @@ msa_status_t msa_invert_selection(const int32_t *sel, const int32_t *q_req, int3
  * CSR entry i = (q, slot) of key (g, req, j) and each head hh < Hq/G of group
  * g, writes the softmax-normalised partial output over block j's tokens at
  * positions <= q_pos[q], and its log-sum-exp (natural log of the sum of exp of
- * the sm_scale-scaled logits), at partial row i (CSR order, so the rows a tile
- * of one key produces are contiguous).  Rows past blk_off[last] are not written.
+ * the sm_scale-scaled logits), as partial i (CSR order).  Entries past
+ * blk_off[last] are not written.
+ *
+ * Partial layout (o_part), HPG = Hq/G.  Entry i owns HPG * D bf16 at element
+ * i * HPG * D, as D/8 column chunks of 8 bf16, chunk-major: the 8 values of
+ * (entry i, head hh, columns 8c .. 8c+7) start at bf16 element
+ *     i * HPG * D  +  (c * HPG + hh) * 8.
+ * This is the order in which the kernel's epilogue stores a tile straight from
+ * registers (one head row per lane: every store instruction writes whole 128-byte
+ * lines).
  *
  *   q        bf16 [n_rows][Hq][D]
  *   k_cache, v_cache bf16 [n_pages][128][G][D]
  *   block_table int32 [n_req][max_blocks];  q_req, q_pos int32 [n_rows]
  *   blk_off, blk_ent  the CSR of msa_invert_selection (same n_req, dims)
- *   o_part   bf16 [n_rows * G * topk][Hq/G][D]  out (entry-major)
+ *   o_part   bf16 [n_rows * G * topk][D/8][Hq/G][8]  out (layout above)
  *   lse_part fp32 [n_rows * G * topk][Hq/G]     out
  *   workspace device scratch of msa_workspace_bytes(MSA_OP_PREFILL, n_rows,
  *            n_req, ...) bytes, 16-byte aligned: the work list (each key cut
@@ -262,14 +270,15 @@ msa_status_t msa_sparse_attn_prefill(const void *q, const void *k_cache, const v
  * msa_lse_merge -- Log-Sum-Exp reduction of per-block partials.  [T-zh KV
  * 块主序稀疏注意力]: the partial O of each KV block is rescaled and summed.  For
  * each (q, h), g = h / (Hq/G), hh = h % (Hq/G), over the slots s with
- * sel[q][g][s] >= 0, the partial O_s / lse_s being row ent_pos[q][g][s], head hh
- * of o_part / lse_part:
+ * sel[q][g][s] >= 0, the partial O_s / lse_s being entry ent_pos[q][g][s], head hh
+ * of o_part (in the layout of msa_sparse_attn_prefill) / lse_part:
  *   lse = m + log(sum_s exp(lse_s - m)),  m = max_s lse_s
  *   out = sum_s exp(lse_s - lse) * O_s
  * Slots with sel < 0 are never read.  An ent_pos outside [0, n_rows*G*topk)
  * raises MSA_FLAG_BOUNDS and that slot is skipped.
  *
- *   o_part   bf16 [n_rows * G * topk][Hq/G][D];  lse_part fp32 [n_rows * G * topk][Hq/G]
+ *   o_part   bf16 [n_rows * G * topk][D/8][Hq/G][8]
+ *   lse_part fp32 [n_rows * G * topk][Hq/G]
  *   sel, ent_pos  int32 [n_rows][G][topk]
  *   out      bf16 [n_rows][Hq][D]  out;  lse fp32 [n_rows][Hq]  out
  */

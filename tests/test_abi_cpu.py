@@ -171,3 +171,27 @@ def test_packed_buffer_layout():
         v.fill_(i + 1)
     for i, v in enumerate(views):
         assert bool((v == i + 1).all())
+
+
+@pytest.mark.parametrize("hpg,D,n_ent", [(8, 128, 37), (4, 64, 70), (8, 64, 16)])
+def test_prefill_partials_layout(hpg, D, n_ent):
+    """The prefill partials buffer and its entry-major view: the value of (entry i, head hh,
+    column col) sits at the bf16 element that msa.h's formula gives, written out here on its
+    own: i * hpg * D + ((col / 8) * hpg + hh) * 8 + col % 8."""
+    import torch
+    import block_sparse_attention_06_gb300 as m
+    shape = m.partials_shape(n_ent, hpg, D)
+    assert shape == (n_ent, D // 8, hpg, 8)
+    flat = torch.zeros(shape, dtype=torch.float64).reshape(-1)
+    for i in range(n_ent):
+        for hh in range(hpg):
+            for col in range(D):
+                at = i * hpg * D + ((col // 8) * hpg + hh) * 8 + col % 8
+                flat[at] = i * 1000 + hh * 100 + col * 0.5
+    em = m.partials_entry_major(flat.reshape(shape), n_ent, hpg, D)
+    want = (torch.arange(n_ent, dtype=torch.float64)[:, None, None] * 1000
+            + torch.arange(hpg, dtype=torch.float64)[None, :, None] * 100
+            + torch.arange(D, dtype=torch.float64)[None, None, :] * 0.5)
+    assert em.shape == (n_ent, hpg, D) and torch.equal(em, want)
+    back = m.partials_from_entry_major(want, hpg, D)   # and the inverse rearrangement
+    assert back.shape == shape and torch.equal(back.reshape(-1), flat)

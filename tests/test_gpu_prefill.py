@@ -268,7 +268,8 @@ def test_lse_merge_matches_oracle(msa):
     o_ent[ent_pos.long().flatten()] = o_g.reshape(-1, hpg, D)
     l_ent[ent_pos.long().flatten()] = l_g.reshape(-1, hpg)
     dims = msa.Dims(Hq, G, D, 64, k, 20)
-    out, l = msa.msa_lse_merge(o_ent.to(DEV), l_ent.to(DEV), sel.to(DEV), ent_pos.to(DEV), dims)
+    o_lay = msa.partials_from_entry_major(o_ent, hpg, D)   # the kernel's partials layout
+    out, l = msa.msa_lse_merge(o_lay.to(DEV), l_ent.to(DEV), sel.to(DEV), ent_pos.to(DEV), dims)
     valid = (sel >= 0).repeat_interleave(Hq // G, dim=1).transpose(1, 2)
     lse_m = torch.where(valid, lse.double(), torch.tensor(float("-inf"), dtype=torch.float64))
     ro, rl = oracle.lse_merge(o.double() * valid[..., None], lse_m)
