@@ -174,14 +174,6 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// This thread's committed bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
-// This thread's committed bulk stores are complete (written to global memory).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Warm L2 with a tile that a later TMA load will fetch.
 __device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2,
                                                    int32_t c3) {
@@ -304,22 +296,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// Shared -> global tiled store, 2-D tensor map.
 // L2 policy for data written once and read back much later (evict first), so a
 // stream of such writes does not push out lines that are read again soon.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-
-// tma_store_2d with an L2 cache policy (l2_policy_evict_first and the like).
-__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, const void *smem_src, int32_t c0,
-                                                  int32_t c1, uint64_t policy) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
-                 ::"l"(reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "l"(policy)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() {
