@@ -33,13 +33,15 @@
 //              The tensor core takes an MMA about when the one before it ends, so
 //              the issuer's own waits are idle tensor time: per tile it waits on
 //              the Q buffer (whose loader has read the tile's descriptor first, so
-//              the flags can be read after it), on one barrier for the previous
-//              tile's P and O buffer together, and on K or V at a chunk's start;
+//              the flags can be read after it), on K or V at a chunk's start, and
+//              for the previous tile's PV twice: once for P of tokens 0..63 and the
+//              O buffer (the first four MMAs), once for the rest of P;
 //   warp 2     K/V loader: K_j by TMA (128B swizzle, 64-column boxes) once the
 //              previous chunk's last S has completed, V_j once its last PV has;
 //   warps 4-7, 8-11  two softmax groups that take alternate tiles: S is read
 //              from TMEM in 32-column chunks twice (row max, then exp2 and P as
-//              packed bf16 written over S); the row's 1/sum goes to a four-slot
+//              packed bf16 written over S, signalled after the first 64 tokens
+//              and again at the end); the row's 1/sum goes to a four-slot
 //              ring in shared memory (so a group never waits for the epilogue to
 //              read the previous one) and its lse to the partials; while one group
 //              runs its softmax the tensor core works on the other group's tile;
@@ -103,7 +105,8 @@ struct AttnSmem {
     uint64_t k_full, k_empty, v_full, v_empty;
     uint64_t q_full[kQBuf], q_empty[kQBuf];
     uint64_t s_full[2], o_full[2];
-    uint64_t pv_ready[2];   // P written by the tile's softmax group and its O buffer read out by the epilogue
+    uint64_t p_lo[2];       // P of tokens 0..63 written (softmax group) and the O buffer read out (epilogue)
+    uint64_t pv_ready[2];   // all of P written by the tile's softmax group
     uint64_t stat_full[4], stat_free[4];            // inv_le[i] written / read by the epilogue
     uint64_t desc_ready[kRing], desc_full[kRing], desc_empty[kRing];
     uint64_t chunk_ready[4], chunk_free[4];
@@ -187,30 +190,6 @@ __device__ __forceinline__ void mma_s_block(uint32_t d, uint64_t a, uint64_t b, 
     }
 }
 
-// Eight MMAs of O = P V (K = 16 tokens each): A = P in TMEM, 8 columns (16 bf16 pairs) per k-step;
-// B = V MN-major 128B-swizzled, 16 rows of 128 bytes per k-step (+128 descriptor units).  Issued by
-// the threads with `leader` set (one thread).  The first MMA overwrites D.
-__device__ __forceinline__ void mma_pv_block(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t leader) {
-    asm volatile(
-        "{\n\t.reg .pred f, t, e;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
-        ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
-        "setp.ne.b32 e, %4, 0;\n\tsetp.ne.b32 f, %4, %4;\n\tsetp.eq.b32 t, %4, %4;\n\t"
-        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\tadd.s32 a4, %1, 32;\n\t"
-        "add.s32 a5, %1, 40;\n\tadd.s32 a6, %1, 48;\n\tadd.s32 a7, %1, 56;\n\t"
-        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\tadd.s64 b4, %2, 512;\n\t"
-        "add.s64 b5, %2, 640;\n\tadd.s64 b6, %2, 768;\n\tadd.s64 b7, %2, 896;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, f;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(leader)
-        : "memory");
-}
-
 // 16-byte global store with an L2 cache policy (l2_policy_evict_first and the like).
 __device__ __forceinline__ void st_global_v4_hint(void *p, const uint32_t (&w)[4], uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(w[0]), "r"(w[1]),
@@ -220,6 +199,22 @@ __device__ __forceinline__ void st_global_v4_hint(void *p, const uint32_t (&w)[4
 
 __device__ __forceinline__ int sm_flags(const TileDesc &d) {
     return *reinterpret_cast<const volatile int32_t *>(&d.flags);
+}
+
+// Four MMAs of O = P V (64 tokens): A = P in TMEM at columns a, a + 8, a + 16, a + 24; B = V at
+// descriptors b, b + 128, b + 256, b + 384.  The first overwrites D when acc == 0.
+__device__ __forceinline__ void mma_pv_half(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 a1, a2, a3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"
+        "add.s32 a1, %1, 8;\n\tadd.s32 a2, %1, 16;\n\tadd.s32 a3, %1, 24;\n\t"
+        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
 }
 
 // Work-list header in the workspace: [0] next chunk (atomic), [1] chunk count.
@@ -318,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         mbar_init(&sm.k_empty, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.s_full[b], 1);
-            mbar_init(&sm.pv_ready[b], 8);   // 4 softmax warps (P) + 4 epilogue warps (O two tiles back)
+            mbar_init(&sm.p_lo[b], 8);       // 4 softmax warps (P, tokens 0..63) + 4 epilogue warps (O)
+            mbar_init(&sm.pv_ready[b], 4);   // 4 softmax warps (all of P)
             mbar_init(&sm.o_full[b], 1);
         }
         mbar_init(&sm.v_full, 1);
@@ -339,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
         for (int b = 0; b < 2; ++b)   // the first tile of each O buffer has no earlier tile to read out
-            for (int i = 0; i < 4; ++i) mbar_arrive(&sm.pv_ready[b]);
+            for (int i = 0; i < 4; ++i) mbar_arrive(&sm.p_lo[b]);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -526,15 +522,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             const uint64_t kd = make_smem_desc(smem_u32(sm.k), 16, 1024, 2);
             const uint64_t vd = make_smem_desc(smem_u32(sm.v), 16384, 1024, 2);
             int cs_k = -1, cs_v = -1;
+            // PV in two halves of 64 tokens: the first as soon as the softmax has written P for tokens
+            // 0..63 (and the O buffer is free), the second once all of P is written, so half of PV runs
+            // while the softmax finishes
             auto issue_pv = [&](int t, int flags) -> bool {
                 const int b = t & 1;
-                if (!mbar_wait(&sm.pv_ready[b], (t >> 1) & 1, err, &sm.abort)) return false;
+                if (!mbar_wait(&sm.p_lo[b], (t >> 1) & 1, err, &sm.abort)) return false;
                 if (flags & kFlagFirst) {
                     ++cs_v;
                     if (!mbar_wait(&sm.v_full, cs_v & 1, err, &sm.abort)) return false;
                 }
                 tc_fence_after();
-                mma_pv_block(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128), vd, kIdescO, 1u);
+                mma_pv_half(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128), vd, kIdescO, 0u);
+                if (!mbar_wait(&sm.pv_ready[b], (t >> 1) & 1, err, &sm.abort)) return false;
+                tc_fence_after();
+                mma_pv_half(tmem + uint32_t(256 + b * D), tmem + uint32_t(b * 128 + 32), vd + 512, kIdescO, 1u);
                 mma_commit(&sm.o_full[b]);
                 if (flags & kFlagLast) mma_commit(&sm.v_empty);
                 return true;
@@ -738,6 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
                     }
                 }
                 tmem_st16(t_s + uint32_t(c >> 1), w);
+                if (c == 32) {   // P of tokens 0..63 is in TMEM: the first half of PV may start
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.p_lo[wg]);
+                }
             }
             const float le = (sum2(acc2[0]) + sum2(acc2[1])) + (sum2(acc2[2]) + sum2(acc2[3]));
             // slot u % 4 is free once the epilogue has read tile u - 4's row sums
@@ -802,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_prefill(
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.pv_ready[b]);   // O buffer b is free for tile u + 2
+            if (lane == 0) mbar_arrive(&sm.p_lo[b]);   // O buffer b is free for tile u + 2
         }
     }
 
